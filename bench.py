@@ -1,0 +1,418 @@
+"""Benchmark of the fused sharded optimizer step on GB300.
+
+Default workload: the GPT-2-Large-shaped ZeRO-1 step (N = 8 simulated ranks,
+38 units, Psi = 774,030,080 parameters, bf16 gradients, fp32 master/m/v, bf16
+gathered params).  One step = one zero_step call = reduce-scatter + average +
+AdamW + bf16 cast + all-gather over every unit, one kernel launch.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+Prints one JSON line (rank 0).  value = parameters updated per second over
+all GPUs (each GPU runs its own full simulated-N-rank step: weak scaling);
+e2e = the same metric with the step's gradients copied in from pinned host
+memory and the gathered params copied back, every step; roofline = the fused
+kernel's algorithmic bytes / its CUDA-event duration against the measured HBM
+copy peak; cpu_baseline = the CPU oracle, single-threaded, on a bounded sample.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sharded-step params/sec and achieved HBM GB/s (% of GB300 peak) at 1 GPU"
+UNIT = "params/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SRC = os.path.join(ROOT, "fsdp_sharded_optimizer_step_gb300", "csrc", "zero_kernels.cu")
+
+
+def kernel_source_hash():
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(workload):
+    """Per-launch DRAM bytes (read + write) of the fused kernel from the committed
+    ncu summary, or None when the summary is missing or the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", f"k_fused_step_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
+    t = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m or not t or m.group(1) != kernel_source_hash():
+        return None
+    return int(t.group(1))
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.samples = []
+        self.proc = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"]
+        except Exception:
+            sel = []
+        self.cmd = ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        self.mark = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.6)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def begin(self):
+        self.mark = time.time()
+
+    def end(self):
+        self.mark_end = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        inside = [p for (t, p) in self.samples if self.mark is not None and self.mark - 0.2 <= t <= self.mark_end + 0.2]
+        use = inside if inside else [p for (_, p) in self.samples]
+        if not use:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in use if num(p[1]) is not None]
+        mx = [num(p[2]) for p in use if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in use for i in range(4) if p[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl != "reference" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    """Largest value of x over all ranks (float)."""
+    if world == 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle (baseline only)
+def oracle_sample_rate(cfg, n_elems, min_seconds, seed=7, max_steps=1000):
+    """The CPU oracle as it stands (single-threaded C), timed on host cores over a
+    bounded sample of the workload: one unsharded step over n_elems positions,
+    repeated until min_seconds have passed.  Returns (params/s, steps, seconds)."""
+    from oracle import oracle as O
+    from fsdp_sharded_optimizer_step_gb300 import workloads as W
+    N = cfg["N"]
+    g = W.make_grads(N, n_elems, cfg["gdtype"], sigma=cfg.get("grad_sigma", 1e-3), device="cpu", seed=seed)
+    rows = ([r for r in g.view(torch.int16).numpy().view(np.uint16)] if cfg["gdtype"] == W.BF16
+            else [r for r in g.numpy()])
+    w = (torch.randn(n_elems, generator=torch.Generator().manual_seed(seed)) * 0.02).numpy()
+    m = np.zeros(n_elems, np.float32)
+    v = np.zeros(n_elems, np.float32)
+    pd = O.BF16 if cfg["pdtype"] == W.BF16 else O.F32
+    gd = O.BF16 if cfg["gdtype"] == W.BF16 else O.F32
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        hp = O.hparams(t=steps + 1, max_norm=cfg.get("max_norm", 0.0))
+        O.step(rows, gd, w, m, v, hp, pdtype=pd)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or steps >= max_steps:
+            return n_elems * steps / el, steps, el
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle, as it stands, on this workload."""
+    if rank != 0:
+        return 0
+    from oracle import build as obuild
+    from fsdp_sharded_optimizer_step_gb300 import workloads as W
+    obuild.build()
+    cfg = W.CONFIGS[args.config]
+    n = args.ref_sample
+    from oracle import oracle as O
+    N = cfg["N"]
+    g = W.make_grads(N, n, cfg["gdtype"], sigma=cfg.get("grad_sigma", 1e-3), device="cpu", seed=7)
+    rows = ([r for r in g.view(torch.int16).numpy().view(np.uint16)] if cfg["gdtype"] == W.BF16
+            else [r for r in g.numpy()])
+    w = (torch.randn(n, generator=torch.Generator().manual_seed(7)) * 0.02).numpy()
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    pd = O.BF16 if cfg["pdtype"] == W.BF16 else O.F32
+    gd = O.BF16 if cfg["gdtype"] == W.BF16 else O.F32
+    for s in range(args.warmup):
+        O.step(rows, gd, w, m, v, O.hparams(t=s + 1, max_norm=cfg.get("max_norm", 0.0)), pdtype=pd)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        O.step(rows, gd, w, m, v, O.hparams(t=args.warmup + s + 1, max_norm=cfg.get("max_norm", 0.0)), pdtype=pd)
+    el = time.perf_counter() - t0
+    value = n * args.steps / el
+    sample = f"{n} positions of the {args.config} workload (N={N} ranks), one unsharded oracle step per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": workload_config(args.config, cfg, None),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(name, cfg, plan):
+    units = cfg["units"]()
+    d = {"workload": f"{name}: {cfg['desc']}", "sim_ranks": cfg["N"], "units": len(units), "psi": int(sum(units)),
+         "grad_dtype": cfg["gdtype"], "param_dtype": cfg["pdtype"], "zero_stage": cfg["stage"],
+         "clip_max_norm": cfg.get("max_norm", 0.0)}
+    if plan is not None:
+        d["p_pad"] = plan.P_pad
+    return d
+
+
+# ------------------------------------------------------------------ the GPU arm
+def update_bytes_per_element(cfg):
+    """Algorithmic HBM bytes per padded element of the update launches of one
+    step: N gradient reads, master/m/v read and written, one param written (the
+    gathered param, or the rank's param shard under ZeRO-3), plus the fp32
+    gradient shard written and read back when clipping."""
+    gb = 2 if cfg["gdtype"] == "bf16" else 4
+    pb = 2 if cfg["pdtype"] == "bf16" else 4
+    b = cfg["N"] * gb + 12 + 12 + pb
+    if cfg.get("max_norm", 0.0) > 0:
+        b += 8
+    return b
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="gpt2l")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--per-unit", action="store_true", help="one launch per unit instead of the multi-unit table")
+    ap.add_argument("--ref-sample", type=int, default=1 << 22)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import fsdp_sharded_optimizer_step_gb300 as Z
+    from fsdp_sharded_optimizer_step_gb300 import build as zbuild
+    from fsdp_sharded_optimizer_step_gb300 import workloads as W
+    zbuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = W.CONFIGS[args.config]
+    sizes = cfg["units"]()
+    N = cfg["N"]
+    plan = Z.ZeroPlan(sizes, N, dev)
+    P, H = plan.P_pad, plan.H
+    gdt = torch.bfloat16 if cfg["gdtype"] == W.BF16 else torch.float32
+    pdt = torch.bfloat16 if cfg["pdtype"] == W.BF16 else torch.float32
+    grads = W.make_grads(N, P, cfg["gdtype"], sigma=cfg.get("grad_sigma", 1e-3), device=dev, seed=1 + 100 * rank,
+                         outlier_frac=cfg.get("outlier_frac", 0.0), outlier_scale=cfg.get("outlier_scale", 1.0),
+                         out=Z.rank_buffers(N, P, gdt, dev))
+    master, m, v = W.make_state(N, H, sigma=cfg.get("master_sigma", 0.02), device=dev,
+                                out=tuple(Z.rank_buffers(N, H, torch.float32, dev) for _ in range(3)))
+    clip = cfg.get("max_norm", 0.0) > 0
+    z3 = cfg["stage"] == 3
+    full = torch.zeros(P, dtype=pdt, device=dev)
+    pshard = Z.rank_buffers(N, H, pdt, dev, zero=True) if z3 else None
+    gshard = Z.rank_buffers(N, H, torch.float32, dev) if clip else None
+    sq = torch.zeros(1, dtype=torch.float64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    units = list(range(plan.n_units)) if args.per_unit else [-1]
+
+    def step(t, ev=None):
+        hp = Z.AdamW(t=t, max_norm=cfg.get("max_norm", 0.0), **W.HP)
+        if ev is not None:
+            ev[0].record(stream)
+        for u in units:
+            Z.zero_step(plan, grads, master, m, v, hp, full=None if z3 else full, pshard=pshard,
+                        gshard_ws=gshard, sqnorm_out=sq if clip else None, unit=u)
+        if ev is not None:
+            ev[1].record(stream)
+        if z3:
+            for u in range(plan.n_units):
+                Z.zero_all_gather_bf16(plan, pshard, full, unit=u)
+
+    launches_per_step = len(units) * (3 if clip else 1) + (plan.n_units if z3 else 0)
+
+    for t in range(1, args.warmup + 1):
+        step(t)
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.begin()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(args.warmup + 1 + k, evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks.end()
+    clock_info = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    ms_per_step = elapsed_ms / args.steps
+    psi = int(sum(sizes))
+    value = world * psi / (ms_per_step / 1e3)
+
+    # the dominant kernel: the update launch(es) of one step, timed on its stream
+    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    bpe = update_bytes_per_element(cfg)  # the ZeRO-3 gathers run outside these events
+    alg_bytes = bpe * P
+    peak, peak_kind = measured_hbm_peak()
+    achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
+    traffic = ncu_traffic(args.config) if not args.per_unit else None
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic, "peak_kind": peak_kind, "bytes_per_element": bpe,
+                "algorithmic_bytes_per_launch": alg_bytes,
+                "kernel": "k_reduce + k_finalize + k_adamw_shard" if clip else "k_fused_step"}
+
+    # ---------------- end to end through the public API with host buffers
+    e2e_steps = max(3, min(args.steps, 10))
+    h_grads = torch.empty(N, P, dtype=gdt, pin_memory=True)
+    for r in range(N):
+        h_grads[r].copy_(grads[r])
+    h_full = torch.empty(P, dtype=pdt, pin_memory=True)
+    torch.cuda.synchronize(dev)
+
+    def e2e_step(t):  # every step: the step's gradients in from pinned host memory, the gathered params out
+        for r in range(N):
+            grads[r].copy_(h_grads[r], non_blocking=True)
+        step(t)
+        h_full.copy_(full, non_blocking=True)
+
+    for t in range(2):  # warm the copy engines
+        e2e_step(10_000 + t)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(e2e_steps):
+        e2e_step(20_000 + k)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    e2e = {"value": world * psi / (e2e_ms / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": h_grads.numel() * h_grads.element_size(),
+           "d2h_bytes_per_step": h_full.numel() * h_full.element_size(), "ms_per_step": e2e_ms, "steps": e2e_steps}
+    del h_grads, h_full
+
+    # ---------------- CPU oracle baseline (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and world == 1:
+        from oracle import build as obuild
+        obuild.build()
+        n_cpu = 1 << 23
+        rate, nsteps, secs = oracle_sample_rate(cfg, n_cpu, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{nsteps} oracle steps over {n_cpu} positions of the {args.config} workload "
+                         f"(N={N} ranks), {secs:.1f} s single-threaded"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": dict(workload_config(args.config, cfg, plan),
+                               l2="inputs larger than L2 (no flush): "
+                                  f"{alg_bytes / 1e9:.1f} GB of HBM traffic per step vs 129 MB of L2",
+                               launch="one launch per unit" if args.per_unit else "one multi-unit launch",
+                               parallelism=f"{world} GPU(s), each a full replica of the {N}-simulated-rank step"),
+                "hbm_gbs": achieved, "pct_of_peak": 100 * achieved / peak,
+                "pct_of_8tbs_nominal": 100 * achieved / 8000.0,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": args.steps * launches_per_step, "clocks": clock_info,
+                "kernel_source_sha256_16": kernel_source_hash(),
+                "device": torch.cuda.get_device_name(dev)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,303 @@
+"""Thin ctypes binding over the C ABI (include/zero.h), with the same names.
+
+Argument marshalling only: tensors become device pointers, rank lists become
+host pointer arrays, streams become cudaStream_t handles; every step of the
+path runs in the CUDA library.  The binding checks what ctypes cannot (device,
+dtype, contiguity, length of every tensor) so that a wrong tensor is refused on
+the host instead of reaching a kernel.  There is no fallback: if the library
+is not built this module raises.
+"""
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+ZERO_OK, ZERO_EINVAL, ZERO_ENOMEM, ZERO_ECUDA, ZERO_EALIGN, ZERO_ENOTATTACHED = 0, -1, -2, -3, -4, -7
+ZERO_F32, ZERO_BF16 = 0, 1
+ZERO_MAX_RANKS = 64
+
+_DTYPES = {torch.float32: ZERO_F32, torch.bfloat16: ZERO_BF16}
+
+
+class ZeroError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        msg = lib().zero_status_string(status).decode()
+        extra = ""
+        if status == ZERO_ECUDA:
+            extra = f" (cudaError {lib().zero_last_cuda_error()})"
+        super().__init__(f"{what}: {msg}{extra} [{status}]")
+
+
+class Hparams(C.Structure):
+    _fields_ = [("lr", C.c_float), ("b1", C.c_float), ("b2", C.c_float), ("eps", C.c_float),
+                ("wd", C.c_float), ("t", C.c_int32), ("max_norm", C.c_float)]
+
+
+@dataclass
+class AdamW:
+    """zero_hparams: AdamW constants, 1-based step t, max_norm > 0 to clip."""
+    lr: float = 0.01
+    b1: float = 0.9
+    b2: float = 0.95
+    eps: float = 1e-8
+    wd: float = 0.1
+    t: int = 1
+    max_norm: float = 0.0
+
+    def c(self) -> Hparams:
+        return Hparams(self.lr, self.b1, self.b2, self.eps, self.wd, int(self.t), self.max_norm)
+
+
+_LIB = None
+SYMBOLS = {}
+
+
+def lib():
+    """Loads the CUDA library (fails loudly when it is not built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"CUDA library {_build.LIB} is missing: build it with "
+                               "fsdp_sharded_optimizer_step_gb300.build.build() (or __graft_entry__.build())")
+        L = C.CDLL(_build.LIB)
+        p, i32, i64, f32 = C.c_void_p, C.c_int32, C.c_int64, C.c_float
+        pp = C.POINTER(C.c_void_p)
+        sig = {
+            "zero_plan_create": (C.c_int, [p, i32, i32, C.POINTER(C.c_void_p)]),
+            "zero_plan_destroy": (None, [p]),
+            "zero_plan_query": (C.c_int, [p, p, p, p, p, p, p]),
+            "zero_plan_counts": (C.c_int, [p, p, p, p]),
+            "zero_plan_segments": (C.c_int, [p, p]),
+            "zero_plan_workspace_bytes": (C.c_int, [p, C.POINTER(C.c_size_t)]),
+            "zero_plan_attach": (C.c_int, [p, p, C.c_size_t, p]),
+            "zero_bias_corrections": (C.c_int, [i32, f32, f32, p, p]),
+            "zero_reduce_scatter": (C.c_int, [p, pp, i32, pp, f32, p]),
+            "zero_grad_sqnorm": (C.c_int, [p, pp, i32, p, p]),
+            "zero_adamw_shard_step": (C.c_int, [p, pp, pp, pp, pp, pp, p, i32, p, p]),
+            "zero_all_gather": (C.c_int, [p, pp, p, i32, i32, p]),
+            "zero_all_gather_bf16": (C.c_int, [p, pp, p, i32, p]),
+            "zero_step": (C.c_int, [p, pp, i32, pp, pp, pp, p, pp, i32, pp, p, p, i32, p]),
+            "zero_status_string": (C.c_char_p, [C.c_int]),
+            "zero_last_cuda_error": (C.c_int, []),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+            SYMBOLS[name] = fn
+        _LIB = L
+    return _LIB
+
+
+def _check(status, what):
+    if status != ZERO_OK:
+        raise ZeroError(status, what)
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return C.c_void_p(stream.cuda_stream)
+    return C.c_void_p(int(stream))
+
+
+# ------------------------------------------------------------------ plan
+def zero_plan_create(unit_sizes, n_ranks):
+    sizes = (C.c_int64 * len(unit_sizes))(*[int(s) for s in unit_sizes])
+    h = C.c_void_p()
+    _check(lib().zero_plan_create(sizes, len(unit_sizes), int(n_ranks), C.byref(h)), "zero_plan_create")
+    return h
+
+
+def zero_plan_destroy(handle):
+    lib().zero_plan_destroy(handle)
+
+
+def zero_plan_counts(handle):
+    u, n, s = C.c_int32(), C.c_int32(), C.c_int64()
+    _check(lib().zero_plan_counts(handle, C.byref(u), C.byref(n), C.byref(s)), "zero_plan_counts")
+    return u.value, n.value, s.value
+
+
+def zero_plan_query(handle):
+    """Layout as python ints / lists: P_pad, H, F, Hoff, S, h."""
+    U, _, _ = zero_plan_counts(handle)
+    P, H = C.c_int64(), C.c_int64()
+    arrs = [(C.c_int64 * max(U, 1))() for _ in range(4)]
+    _check(lib().zero_plan_query(handle, C.byref(P), C.byref(H), *arrs), "zero_plan_query")
+    F, Hoff, S, h = ([int(a[i]) for i in range(U)] for a in arrs)
+    return dict(P_pad=P.value, H=H.value, F=F, Hoff=Hoff, S=S, h=h)
+
+
+def zero_plan_segments(handle):
+    """Launch table as a list of (full_pos, shard_pos, len, valid, rank, unit)."""
+    _, _, nseg = zero_plan_counts(handle)
+    out = (C.c_int64 * max(6 * nseg, 1))()
+    _check(lib().zero_plan_segments(handle, out), "zero_plan_segments")
+    return [tuple(out[6 * i:6 * i + 6]) for i in range(nseg)]
+
+
+def zero_plan_workspace_bytes(handle):
+    b = C.c_size_t()
+    _check(lib().zero_plan_workspace_bytes(handle, C.byref(b)), "zero_plan_workspace_bytes")
+    return b.value
+
+
+def zero_plan_attach(handle, workspace: torch.Tensor, stream=None):
+    _check(lib().zero_plan_attach(handle, C.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
+                                  _stream(stream, workspace.device)), "zero_plan_attach")
+
+
+def zero_bias_corrections(t, b1=0.9, b2=0.95):
+    bc1, bc2 = C.c_float(), C.c_float()
+    _check(lib().zero_bias_corrections(int(t), b1, b2, C.byref(bc1), C.byref(bc2)), "zero_bias_corrections")
+    return bc1.value, bc2.value
+
+
+class ZeroPlan:
+    """Owns a plan and its device workspace (a torch uint8 tensor on `device`).
+
+    device=None builds the host-side plan only (layout queries work without a
+    GPU; device calls then fail with ZERO_ENOTATTACHED)."""
+
+    def __init__(self, unit_sizes, n_ranks, device=None, stream=None):
+        self.unit_sizes = [int(s) for s in unit_sizes]
+        self.n_ranks = int(n_ranks)
+        self.handle = zero_plan_create(self.unit_sizes, self.n_ranks)
+        q = zero_plan_query(self.handle)
+        self.P_pad, self.H = q["P_pad"], q["H"]
+        self.F, self.Hoff, self.S, self.h = q["F"], q["Hoff"], q["S"], q["h"]
+        self.n_units, _, self.n_segments = zero_plan_counts(self.handle)
+        self.device = None
+        self.workspace = None
+        if device is not None:
+            self.device = torch.device(device)
+            nbytes = zero_plan_workspace_bytes(self.handle)
+            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+            zero_plan_attach(self.handle, self.workspace, stream)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and _LIB is not None:
+            zero_plan_destroy(h)
+            self.handle = None
+
+
+# ------------------------------------------------------------------ allocation helper
+def rank_buffers(n_ranks, length, dtype, device, zero=False):
+    """[n_ranks, length] view whose rows start 16-byte aligned (the row stride
+    is padded to a multiple of 16 bytes), as the C ABI requires of every rank
+    buffer."""
+    per16 = 16 // torch.empty((), dtype=dtype).element_size()
+    stride = (length + per16 - 1) // per16 * per16
+    alloc = torch.zeros if zero else torch.empty
+    return alloc(n_ranks, max(stride, 1), dtype=dtype, device=device)[:, :length]
+
+
+# ------------------------------------------------------------------ tensor marshalling
+def _rows(plan, x, length, what, dtypes):
+    """A [N, length] tensor or a list of N 1-D tensors -> host array of N device pointers, dtype code."""
+    rows = list(x.unbind(0)) if isinstance(x, torch.Tensor) else list(x)
+    if len(rows) != plan.n_ranks:
+        raise ValueError(f"{what}: expected {plan.n_ranks} rank buffers, got {len(rows)}")
+    dt = rows[0].dtype
+    for r in rows:
+        if r.device != plan.device:
+            raise ValueError(f"{what}: tensor on {r.device}, plan on {plan.device}")
+        if r.dtype != dt or dt not in dtypes:
+            raise ValueError(f"{what}: dtype {r.dtype} not allowed")
+        if r.dim() != 1 or not r.is_contiguous() or r.numel() != length:
+            raise ValueError(f"{what}: each rank buffer must be contiguous 1-D of {length} elements")
+    arr = (C.c_void_p * len(rows))(*[r.data_ptr() for r in rows])
+    return arr, _DTYPES[dt]
+
+
+def _one(plan, x, length, what, dtypes):
+    if x.device != plan.device or x.dtype not in dtypes or not x.is_contiguous() or x.numel() != length:
+        raise ValueError(f"{what}: need a contiguous {length}-element tensor of {dtypes} on {plan.device}")
+    return C.c_void_p(x.data_ptr()), _DTYPES[x.dtype]
+
+
+_G = (torch.bfloat16, torch.float32)
+_F = (torch.float32,)
+
+
+def zero_reduce_scatter(plan, grads, gshard, coef=1.0, stream=None):
+    g, gd = _rows(plan, grads, plan.P_pad, "grads", _G)
+    gs, _ = _rows(plan, gshard, plan.H, "gshard", _F)
+    _check(lib().zero_reduce_scatter(plan.handle, g, gd, gs, float(coef), _stream(stream, plan.device)),
+           "zero_reduce_scatter")
+
+
+def zero_grad_sqnorm(plan, grads, sqnorm_out, stream=None):
+    g, gd = _rows(plan, grads, plan.P_pad, "grads", _G)
+    if sqnorm_out.device != plan.device or sqnorm_out.dtype != torch.float64 or sqnorm_out.numel() < 1:
+        raise ValueError("sqnorm_out: need a float64 tensor on the plan's device")
+    _check(lib().zero_grad_sqnorm(plan.handle, g, gd, C.c_void_p(sqnorm_out.data_ptr()), _stream(stream, plan.device)),
+           "zero_grad_sqnorm")
+
+
+def _outputs(plan, full, pshard):
+    pdt = None
+    fp = None
+    if full is not None:
+        fp, pdt = _one(plan, full, plan.P_pad, "full", _G)
+    ps = None
+    if pshard is not None:
+        ps, d = _rows(plan, pshard, plan.H, "pshard", _G)
+        if pdt is not None and d != pdt:
+            raise ValueError("full and pshard must have the same dtype")
+        pdt = d
+    return fp, ps, (ZERO_BF16 if pdt is None else pdt)
+
+
+def zero_adamw_shard_step(plan, gshard, master, m, v, hp: AdamW, pshard=None, full=None, stream=None):
+    gs, _ = _rows(plan, gshard, plan.H, "gshard", _F)
+    W, _ = _rows(plan, master, plan.H, "master", _F)
+    M, _ = _rows(plan, m, plan.H, "m", _F)
+    V, _ = _rows(plan, v, plan.H, "v", _F)
+    fp, ps, pdt = _outputs(plan, full, pshard)
+    c = hp.c()
+    _check(lib().zero_adamw_shard_step(plan.handle, gs, W, M, V, ps, fp, pdt, C.byref(c), _stream(stream, plan.device)),
+           "zero_adamw_shard_step")
+
+
+def zero_all_gather(plan, shards, full, unit=-1, stream=None):
+    s, sd = _rows(plan, shards, plan.H, "shards", _G)
+    fp, fd = _one(plan, full, plan.P_pad, "full", _G)
+    if sd != fd:
+        raise ValueError("shards and full must have the same dtype")
+    _check(lib().zero_all_gather(plan.handle, s, fp, fd, int(unit), _stream(stream, plan.device)), "zero_all_gather")
+
+
+def zero_all_gather_bf16(plan, shards, full, unit=-1, stream=None):
+    s, sd = _rows(plan, shards, plan.H, "shards", (torch.bfloat16,))
+    fp, _ = _one(plan, full, plan.P_pad, "full", (torch.bfloat16,))
+    _check(lib().zero_all_gather_bf16(plan.handle, s, fp, int(unit), _stream(stream, plan.device)),
+           "zero_all_gather_bf16")
+
+
+def zero_step(plan, grads, master, m, v, hp: AdamW, full=None, pshard=None, gshard_ws=None, sqnorm_out=None,
+              unit=-1, stream=None):
+    """The fused sharded step (see include/zero.h)."""
+    g, gd = _rows(plan, grads, plan.P_pad, "grads", _G)
+    W, _ = _rows(plan, master, plan.H, "master", _F)
+    M, _ = _rows(plan, m, plan.H, "m", _F)
+    V, _ = _rows(plan, v, plan.H, "v", _F)
+    fp, ps, pdt = _outputs(plan, full, pshard)
+    gs = None
+    if gshard_ws is not None:
+        gs, _ = _rows(plan, gshard_ws, plan.H, "gshard_ws", _F)
+    sq = None
+    if sqnorm_out is not None:
+        if sqnorm_out.device != plan.device or sqnorm_out.dtype != torch.float64:
+            raise ValueError("sqnorm_out: need a float64 tensor on the plan's device")
+        sq = C.c_void_p(sqnorm_out.data_ptr())
+    c = hp.c()
+    _check(lib().zero_step(plan.handle, g, gd, W, M, V, fp, ps, pdt, gs, C.byref(c), sq, int(unit),
+                           _stream(stream, plan.device)), "zero_step")

@@ -1,0 +1,65 @@
+// Internal types shared by the host plan (zero_plan.cpp) and the kernels
+// (zero_kernels.cu).  Not part of the C ABI.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include "../../include/zero.h"
+
+namespace zero {
+
+// One work segment: a contiguous run of one rank's slice of one unit.  The
+// multi-unit launch table lists every segment of every (unit, rank) slice,
+// ordered by unit, then rank, then position; a kernel launch maps one CTA to
+// one segment, so thousands of small units cost one launch, not thousands.
+struct Seg {
+    int64_t g_off;  // full-buffer position of the segment's first element: F_u + r*h_u + j0
+    int64_t s_off;  // shard-buffer position of the same element: Hoff_u + j0
+    int32_t len;    // elements in the segment (1..kSegMax)
+    int32_t valid;  // elements before the unit's padding starts (0..len)
+    int32_t rank;
+    int32_t unit;
+};
+static_assert(sizeof(Seg) == 32, "Seg must stay 32 bytes");
+
+// Longest segment.  Segments after the first one of a slice start at a shard
+// position that is a multiple of 8, so 32-byte vector access needs no peeling.
+constexpr int32_t kSegMax = 32768;
+
+// The binary32 constants of one AdamW step, computed once on the host
+// (compiled without FMA contraction) from zero_hparams.
+struct AdamConsts {
+    float b1, b2;
+    float omb1, omb2;  // 1 - b1, 1 - b2
+    float decay;       // 1 - lr*wd
+    float lr_bc1;      // lr / bc1
+    float bc2, eps;
+};
+
+}  // namespace zero
+
+struct zero_plan {
+    int32_t n_units = 0, n_ranks = 0;
+    std::vector<int64_t> sizes, S, h, F, Hoff;
+    int64_t p_pad = 0, H = 0;
+    std::vector<zero::Seg> segs;           // host copy of the launch table
+    std::vector<int64_t> unit_seg_begin;   // [n_units + 1]: segments of unit u
+    // device side, set by zero_plan_attach
+    bool attached = false;
+    int device = -1;
+    zero::Seg *d_segs = nullptr;
+    double *d_partials = nullptr;   // one binary64 partial sum per segment
+    double *d_sqnorm = nullptr;     // S of the last clipped step
+    float *d_coef = nullptr;        // clip coefficient of the last clipped step
+};
+
+namespace zero {
+// Workspace layout (byte offsets from the workspace base).
+struct WsLayout {
+    size_t segs, partials, scalars, total;
+};
+WsLayout workspace_layout(const zero_plan *plan);
+int adam_consts(const zero_hparams *hp, AdamConsts *out);
+void set_last_cuda_error(int code);
+}  // namespace zero

@@ -116,15 +116,18 @@ def make_grads(n_ranks, length, dtype=BF16, sigma=1e-3, device="cpu", seed=1, ou
     return out
 
 
-def make_state(n_ranks, length, sigma=0.02, device="cpu", seed=1000):
-    """Per-rank fp32 master ~ N(0, sigma^2) and zero m, v, each [n_ranks, length]."""
+def make_state(n_ranks, length, sigma=0.02, device="cpu", seed=1000, out=None):
+    """Per-rank fp32 master ~ N(0, sigma^2) and zero m, v, each [n_ranks, length]
+    (written into `out` = (master, m, v) when given)."""
     gen = _gen(device, seed)
-    master = torch.empty(n_ranks, length, dtype=torch.float32, device=device)
+    if out is None:
+        out = tuple(torch.empty(n_ranks, length, dtype=torch.float32, device=device) for _ in range(3))
+    master, m, v = out
     chunk = 1 << 28
     for r in range(n_ranks):
         for s in range(0, length, chunk):
             e = min(length, s + chunk)
             master[r, s:e] = torch.randn(e - s, generator=gen, device=device, dtype=torch.float32) * sigma
-    m = torch.zeros_like(master)
-    v = torch.zeros_like(master)
+    m.zero_()
+    v.zero_()
     return master, m, v

@@ -1,0 +1,229 @@
+/*
+ * zero.h -- C ABI of the GB300 sharded optimizer step (ZeRO-1/2/3 update).
+ *
+ * What the library computes.  N data-parallel ranks each hold a full padded
+ * gradient buffer.  The gradients are reduce-scattered (summed over ranks in
+ * rank order, divided by N): rank r receives slice r of every unit.  Each
+ * rank runs AdamW on its own fp32 master/m/v slice, casts the result to bf16
+ * and all-gathers it into the full parameter buffer.  An optional global
+ * gradient-norm clip scales the averaged gradient first.
+ *   - "ZeRO and FSDP sharding", How it works: per-unit flat buffers padded to a
+ *     multiple of N, rank r owns slice r; the step is AdamW on the fp32 master
+ *     slice, a cast to bf16, and one all-gather of the updated params.
+ *   - "ZeRO and FSDP sharding", Code: the reduce-scatter, the division by n,
+ *     AdamW::step and the all-gather; the sharded result equals unsharded
+ *     AdamW on the averaged gradient bit for bit.
+ *   - "ZeRO: Three Ledgers, Zero Redundancy", section 2: all-reduce =
+ *     reduce-scatter + local update + all-gather; the clip norm is a
+ *     decomposable sum of squares.
+ *   - "ZeRO and FSDP sharding", Implementation notes: clipping needs the global
+ *     norm; gradients reduced in fp32, weights gathered in bf16.
+ *
+ * The N ranks live on ONE GPU as N resident HBM buffers: rank q's "send
+ * buffer" is its gradient buffer, the reduce-scatter is a kernel that reads
+ * all N buffers at the same offset, and the all-gather is the same kernel
+ * writing the rank's slice into the full buffer.
+ *
+ * Arithmetic: every float operation of the update is one IEEE binary32
+ * operation rounded to nearest even, in the order
+ *     g = (((g_0 + g_1) + g_2) + ... + g_{N-1}) / N          [* coef]
+ *     m = (b1*m) + ((1-b1)*g)
+ *     v = (b2*v) + (((1-b2)*g)*g)
+ *     w = (w*(1-lr*wd)) - (((lr/bc1)*m) / ((sqrt(v)/bc2) + eps))
+ *     bc1 = 1 - b1^t, bc2 = sqrt(1 - b2^t), b^t by binary exponentiation in
+ *     binary32 (computed on the host, once per call),
+ * and the bf16 output is w rounded to nearest even (a NaN stays a NaN with its
+ * sign).  Results are bit-identical to that sequence; nothing is fused.
+ *
+ * Layout (all counts in elements).  For unit u of s_u parameters:
+ *   S_u = s_u rounded up to a multiple of N, h_u = S_u / N,
+ *   F_u = sum_{k<u} S_k (unit offset in the full buffer),
+ *   Hoff_u = sum_{k<u} h_k (unit offset in every rank's shard buffer),
+ *   P_pad = sum S_u, H = P_pad / N.
+ * Rank r owns full positions [F_u + r*h_u, F_u + (r+1)*h_u) of unit u, stored
+ * at [Hoff_u, Hoff_u + h_u) of its shard buffers.  Gradient and full buffers
+ * have P_pad elements; master/m/v/param-shard/grad-shard buffers have H.
+ * Full positions F_u + k with k >= s_u are padding: their gradient entries are
+ * never read (they count as 0), and the update runs on them like on any other
+ * position (pads initialised to 0 stay exactly 0).
+ *
+ * Conventions.
+ *   - Every function returns a status (ZERO_OK = 0, negative on error) and
+ *     checks all arguments on the host before anything is launched; on error
+ *     nothing is launched and no memory is touched.
+ *   - The caller owns all device memory and streams (PyTorch allocates them).
+ *     The library owns only the opaque plan (host memory); its device tables
+ *     live in a caller-provided workspace (zero_plan_attach).
+ *   - Device work is asynchronous on the given stream (NULL = legacy default
+ *     stream).  Calls that use the same plan's workspace must be ordered on one
+ *     stream, or otherwise serialised by the caller.
+ *   - Arrays of rank pointers ("[N]") are HOST arrays of N DEVICE pointers.
+ *     Every device pointer must be 16-byte aligned (ZERO_EALIGN otherwise).
+ *   - A plan is immutable after zero_plan_attach and may be shared by threads
+ *     that serialise their device work.
+ */
+#ifndef ZERO_H
+#define ZERO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct zero_plan zero_plan;
+typedef struct CUstream_st *zero_stream_t; /* the same type as cudaStream_t */
+
+enum {
+    ZERO_OK = 0,
+    ZERO_EINVAL = -1,      /* a bad argument (null, out of range, wrong dtype, size mismatch) */
+    ZERO_ENOMEM = -2,      /* host allocation failed, or the workspace is too small */
+    ZERO_ECUDA = -3,       /* a CUDA runtime call failed (launch, copy, device query) */
+    ZERO_EALIGN = -4,      /* a device pointer is not 16-byte aligned */
+    ZERO_ENOTATTACHED = -7 /* the plan has no device workspace yet (zero_plan_attach) */
+};
+
+enum { ZERO_F32 = 0, ZERO_BF16 = 1 };
+
+#define ZERO_MAX_RANKS 64
+
+/* AdamW hyper-parameters of one step ("ZeRO and FSDP sharding", Code,
+ * AdamW::step).  t is the 1-based step number.  max_norm > 0 turns on the
+ * global-norm clip: coef = min(1, max_norm / (sqrt(S) + 1e-6)) in binary64,
+ * rounded once to binary32, where S is the sum of squares of the averaged
+ * gradient over all ranks and positions (pads count 0). */
+typedef struct {
+    float lr, b1, b2, eps, wd;
+    int32_t t;
+    float max_norm;
+} zero_hparams;
+
+/* ---------------------------------------------------------------- plan */
+
+/* Build the padded layout of n_units units for n_ranks simulated ranks
+ * ("ZeRO and FSDP sharding", How it works and Pitfalls: pad each flat unit
+ * to a multiple of N).  Host only; needs no GPU.  unit_sizes: host array of
+ * n_units non-negative counts (zero-sized units are allowed).  1 <= n_ranks
+ * <= ZERO_MAX_RANKS.  On success *out owns a plan freed by zero_plan_destroy.
+ * Errors: ZERO_EINVAL (bad sizes, n_ranks out of range, total beyond 2^62),
+ * ZERO_ENOMEM. */
+int zero_plan_create(const int64_t *unit_sizes, int32_t n_units, int32_t n_ranks, zero_plan **out);
+
+/* Frees the plan (host memory only; the caller frees its workspace). NULL is a no-op. */
+void zero_plan_destroy(zero_plan *plan);
+
+/* Layout query.  Scalars and arrays are HOST memory; every pointer may be NULL.
+ * p_pad, h: P_pad and H.  F, Hoff, S, h_u: arrays of n_units (unit offsets in
+ * the full buffer, in the shard buffers, padded sizes, slice lengths). */
+int zero_plan_query(const zero_plan *plan, int64_t *p_pad, int64_t *h, int64_t *F, int64_t *Hoff,
+                    int64_t *S, int64_t *h_u);
+
+/* Counts: units, ranks, and the number of work segments of the multi-unit
+ * launch table (a segment is a contiguous run of one rank's slice). */
+int zero_plan_counts(const zero_plan *plan, int32_t *n_units, int32_t *n_ranks, int64_t *n_segments);
+
+/* The launch table, for inspection: out (HOST, 6 * n_segments int64) receives
+ * per segment {full position, shard position, length, valid (non-pad) length,
+ * rank, unit}.  Segments are ordered by unit, then rank, then position. */
+int zero_plan_segments(const zero_plan *plan, int64_t *out);
+
+/* Bytes of device workspace the plan needs (work table, per-segment partial
+ * sums, scalars). Host only. */
+int zero_plan_workspace_bytes(const zero_plan *plan, size_t *bytes);
+
+/* Binds the plan to the current device: copies its work table into the
+ * caller's device workspace (>= zero_plan_workspace_bytes bytes, 256-byte
+ * aligned) on `stream`.  The workspace must outlive every later call with
+ * this plan.  Call once, before any stream capture.  Errors: ZERO_EINVAL (NULL,
+ * already attached), ZERO_ENOMEM (too small), ZERO_EALIGN, ZERO_ECUDA. */
+int zero_plan_attach(zero_plan *plan, void *workspace, size_t bytes, zero_stream_t stream);
+
+/* The host recipe for the bias corrections (t >= 1): bc1 = 1 - b1^t,
+ * bc2 = sqrt(1 - b2^t), b^t by binary exponentiation in binary32.  Every
+ * device call below uses exactly these values. */
+int zero_bias_corrections(int32_t t, float b1, float b2, float *bc1, float *bc2);
+
+/* ---------------------------------------------------------------- steps of the path */
+
+/* Reduce-scatter + average ("ZeRO and FSDP sharding", Code: reduce_scatter,
+ * then /= n): gshard[r][Hoff_u + j] = (sum_q grads[q][F_u + r h_u + j]) / N
+ * (rank-ordered fold, fp32), times coef when coef != 1 (pass 1.0f for none).
+ * grads: [N] device buffers of P_pad elements of gdtype (ZERO_BF16 or
+ * ZERO_F32).  gshard: [N] device fp32 buffers of H elements (output).
+ * Pads of a unit write 0. */
+int zero_reduce_scatter(const zero_plan *plan, const void *const *grads, int32_t gdtype,
+                        float *const *gshard, float coef, zero_stream_t stream);
+
+/* Global squared gradient norm ("ZeRO and FSDP sharding", Implementation
+ * notes; "ZeRO: Three Ledgers, Zero Redundancy", section 2): writes
+ * S = sum over all positions of g^2 (g the averaged gradient, pads 0) as a
+ * binary64 to *sqnorm_dev (DEVICE pointer, 8-byte aligned), asynchronously.
+ * Each segment's partial sum goes to the plan's workspace, then one fixed-order
+ * pass adds them: the result is deterministic, within a few binary64 ulps of
+ * the exact sum. */
+int zero_grad_sqnorm(const zero_plan *plan, const void *const *grads, int32_t gdtype,
+                     double *sqnorm_dev, zero_stream_t stream);
+
+/* Local AdamW on every rank's shard ("ZeRO and FSDP sharding", Code,
+ * AdamW::step; How it works: AdamW on the fp32 master slice, cast to bf16
+ * shard) from an already averaged fp32 gradient shard.  gshard, master, m, v:
+ * [N] device fp32 buffers of H elements; master/m/v are updated in place.
+ * Outputs, each optional (NULL): pshard [N] device buffers of H elements of
+ * pdtype (the rank's param shard), full: a device buffer of P_pad elements of
+ * pdtype (the gathered params, written directly).  No clipping is applied
+ * (hp->max_norm is ignored). */
+int zero_adamw_shard_step(const zero_plan *plan, const float *const *gshard, float *const *master,
+                          float *const *m, float *const *v, void *const *pshard, void *full,
+                          int32_t pdtype, const zero_hparams *hp, zero_stream_t stream);
+
+/* All-gather ("ZeRO and FSDP sharding", Code: all_gather = concatenation of
+ * the shards; How it works: ZeRO-3 gathers per unit): full[F_u + r h_u + j] =
+ * shard[r][Hoff_u + j] for every rank r, for unit `unit`, or every unit when
+ * unit == -1.  shard: [N] device buffers of H elements, full: P_pad elements,
+ * both of pdtype. */
+int zero_all_gather(const zero_plan *plan, const void *const *shard, void *full, int32_t pdtype,
+                    int32_t unit, zero_stream_t stream);
+
+/* zero_all_gather with pdtype = ZERO_BF16. */
+int zero_all_gather_bf16(const zero_plan *plan, const uint16_t *const *shard16, uint16_t *full,
+                         int32_t unit, zero_stream_t stream);
+
+/* The fused sharded step ("ZeRO: Three Ledgers, Zero Redundancy", section 2:
+ * stop the all-reduce halfway and do the update in the middle):
+ * reduce-scatter + average + AdamW + cast + all-gather in ONE pass over the
+ * multi-unit work table (one kernel launch), each gradient byte read once.
+ *   grads   [N] device, P_pad elements of gdtype; read only.
+ *   master, m, v  [N] device fp32, H elements; updated in place.
+ *   full    device, P_pad elements of pdtype, or NULL (ZeRO-1/2 gather target).
+ *   pshard  [N] device, H elements of pdtype, or NULL (ZeRO-3 param shards).
+ *   gshard_ws [N] device fp32, H elements: required when hp->max_norm > 0
+ *           (it then receives the averaged, unclipped gradient shard), else
+ *           ignored (may be NULL).
+ *   sqnorm_dev  DEVICE binary64 or NULL: receives S when clipping.
+ *   unit    -1: all units in one launch; u >= 0: unit u only (no clipping).
+ * With clipping the step is three launches (sum of squares and gradient
+ * shard; fixed-order total and coefficient on the device; update), with no
+ * host synchronisation.  If S is not finite the update is skipped entirely:
+ * master, m, v and the outputs are left untouched, and S (inf or NaN) is still
+ * written to sqnorm_dev so the caller can see it.
+ * Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ENOTATTACHED, ZERO_ECUDA. */
+int zero_step(const zero_plan *plan, const void *const *grads, int32_t gdtype, float *const *master,
+              float *const *m, float *const *v, void *full, void *const *pshard, int32_t pdtype,
+              float *const *gshard_ws, const zero_hparams *hp, double *sqnorm_dev, int32_t unit,
+              zero_stream_t stream);
+
+/* ---------------------------------------------------------------- diagnostics */
+
+/* Static text for a status code. */
+const char *zero_status_string(int status);
+
+/* The last CUDA error code this thread saw inside the library (0 if none),
+ * for callers that got ZERO_ECUDA. */
+int zero_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_H */

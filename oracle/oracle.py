@@ -38,6 +38,8 @@ def lib():
             "orc_plan": (C.c_int, [p, i32, i32, p, p, p, p, p]),
             "orc_shard_map": (C.c_int, [p, i32, i32, p]),
             "orc_pad_mask": (C.c_int, [p, i32, i32, p]),
+            "orc_locate": (C.c_int, [p, i32, i32, i64, p, p, p, p]),
+            "orc_avg_grad_array": (C.c_int, [i64, i32, p, i32, p, p]),
             "orc_bf16_rne": (C.c_uint16, [f32]),
             "orc_bf16_rne_array": (None, [i64, p, p]),
             "orc_bf16_to_f32": (f32, [C.c_uint16]),
@@ -90,6 +92,16 @@ class Plan:
         out = np.zeros(self.N * self.H, np.int64)
         _check(lib().orc_shard_map(_ptr(self.sizes), len(self.sizes), self.N, _ptr(out)), "shard_map")
         return out.reshape(self.N, self.H)
+
+    def locate(self, pos):
+        """(rank, shard position, is_pad) of each full-buffer position in `pos`."""
+        pos = np.ascontiguousarray(pos, np.int64)
+        rank = np.zeros(pos.size, np.int32)
+        spos = np.zeros(pos.size, np.int64)
+        pad = np.zeros(pos.size, np.uint8)
+        _check(lib().orc_locate(_ptr(self.sizes), len(self.sizes), self.N, pos.size, _ptr(pos), _ptr(rank), _ptr(spos),
+                                _ptr(pad)), "locate")
+        return rank, spos, pad
 
     def pad_mask(self):
         out = np.zeros(self.P_pad, np.uint8)
@@ -146,6 +158,14 @@ def sqnorm(grads, gdtype, pad=None) -> float:
 
 
 # ---------------------------------------------------------------- update
+def avg_grad(grads, gdtype, pad=None):
+    """The rank-ordered averaged gradient at every given position."""
+    grads, arr = _grad_ptrs(grads, gdtype)
+    out = np.zeros(grads[0].size, np.float32)
+    _check(lib().orc_avg_grad_array(out.size, len(grads), arr, gdtype, _ptr(pad), _ptr(out)), "avg_grad")
+    return out
+
+
 def _grad_ptrs(grads, gdtype):
     want = np.float32 if gdtype == F32 else np.uint16
     grads = [np.ascontiguousarray(g, dtype=want) for g in grads]

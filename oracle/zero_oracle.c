@@ -114,6 +114,35 @@ int orc_pad_mask(const int64_t *sizes, int32_t n_units, int32_t n_ranks, uint8_t
     return ORC_OK;
 }
 
+/* For n full-buffer positions: the owning rank, the position inside that
+ * rank's shard buffer, and whether the position is padding.  (Searches the
+ * units in order; the same layout as orc_plan.) */
+int orc_locate(const int64_t *sizes, int32_t n_units, int32_t n_ranks, int64_t n, const int64_t *pos,
+               int32_t *rank, int64_t *shard_pos, uint8_t *is_pad)
+{
+    if (n_units < 0 || n_ranks < 1 || n < 0) return ORC_EINVAL;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t f = 0, hh = 0;
+        int found = 0;
+        for (int32_t u = 0; u < n_units && !found; ++u) {
+            int64_t rem = sizes[u] % n_ranks;
+            int64_t Su = rem == 0 ? sizes[u] : sizes[u] + (n_ranks - rem);
+            int64_t hu = Su / n_ranks;
+            if (pos[i] >= f && pos[i] < f + Su) {
+                int64_t k = pos[i] - f;
+                rank[i] = (int32_t)(k / hu);
+                shard_pos[i] = hh + k % hu;
+                is_pad[i] = (uint8_t)(k >= sizes[u]);
+                found = 1;
+            }
+            f += Su;
+            hh += hu;
+        }
+        if (!found) return ORC_EINVAL;
+    }
+    return ORC_OK;
+}
+
 /* ------------------------------------------------------------------------ */
 /* bfloat16.  [P1] How it works: "cast to bf16 shard"; [P4] section 3: the
  * bf16 working copy is a rounded view of the fp32 master.  Reading: round to
@@ -189,6 +218,15 @@ static float orc_avg_grad(int32_t n_ranks, const void *const *grads, int32_t gdt
     float acc = orc_load_grad(grads[0], gdtype, i);
     for (int32_t q = 1; q < n_ranks; ++q) acc = acc + orc_load_grad(grads[q], gdtype, i);
     return acc / (float)n_ranks;
+}
+
+/* The averaged gradient itself at n positions (the reduce-scatter's output). */
+int orc_avg_grad_array(int64_t n, int32_t n_ranks, const void *const *grads, int32_t gdtype,
+                       const uint8_t *pad, float *out)
+{
+    if (n < 0 || n_ranks < 1 || (gdtype != ORC_F32 && gdtype != ORC_BF16)) return ORC_EINVAL;
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_avg_grad(n_ranks, grads, gdtype, pad, i);
+    return ORC_OK;
 }
 
 /* ------------------------------------------------------------------------ */

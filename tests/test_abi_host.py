@@ -1,0 +1,151 @@
+"""Host-side tests of the C ABI (no GPU): the library loads and exports every
+declared symbol; the plan's layout and launch table are integer-exact against
+the oracle; the host bias corrections match the oracle bit for bit; argument
+errors are reported before anything touches a device."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import fsdp_sharded_optimizer_step_gb300 as Z
+from fsdp_sharded_optimizer_step_gb300 import binding as B
+from fsdp_sharded_optimizer_step_gb300 import build as zbuild
+from fsdp_sharded_optimizer_step_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "zero.h")
+
+
+@pytest.fixture(scope="module")
+def zlib():
+    zbuild.build()
+    return Z.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(zero_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(zlib):
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(zlib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", zbuild.LIB], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r" T (zero_[a-z0-9_]+)", out))
+    assert set(names) <= exported
+    # the binding wraps every declared function under the same name
+    for n in names:
+        assert n in B.SYMBOLS or n in ("zero_plan_segments",), n
+        assert hasattr(B, n) or n in ("zero_status_string", "zero_last_cuda_error"), n
+
+
+def _units_cases():
+    rng = np.random.default_rng(0)
+    cases = [([1000], 4), ([0], 3), ([], 5), ([1], 16), ([1, 2, 3], 64), ([7, 0, 13, 1, 64], 8)]
+    for _ in range(40):
+        U = int(rng.integers(1, 20))
+        sizes = rng.integers(0, 200000, U)
+        sizes[rng.random(U) < 0.15] = int(rng.integers(0, 20))
+        cases.append((sizes.tolist(), int(rng.choice([1, 2, 3, 4, 5, 7, 8, 12, 16, 31, 64]))))
+    return cases
+
+
+@pytest.mark.parametrize("sizes,N", _units_cases())
+def test_plan_layout_matches_oracle(zlib, orc, sizes, N):
+    p = Z.ZeroPlan(sizes, N)
+    o = orc.Plan(sizes, N)
+    assert p.P_pad == o.P_pad and p.H == o.H
+    assert p.F == o.F.tolist() and p.Hoff == o.Hoff.tolist() and p.S == o.S.tolist() and p.h == o.h.tolist()
+
+
+@pytest.mark.parametrize("sizes,N", _units_cases()[:20])
+def test_launch_table_covers_every_slice_once(zlib, orc, sizes, N):
+    p = Z.ZeroPlan(sizes, N)
+    segs = Z.zero_plan_segments(p.handle)
+    o = orc.Plan(sizes, N)
+    if o.P_pad == 0:
+        assert segs == []
+        return
+    covered = np.zeros(o.P_pad, np.int32)
+    mp = o.shard_map()
+    pad = o.pad_mask()
+    for (g, s, ln, valid, r, u) in segs:
+        assert 1 <= ln <= 32768 and 0 <= valid <= ln
+        covered[g:g + ln] += 1
+        # the segment's full positions are exactly rank r's shard positions s..s+ln
+        assert np.array_equal(mp[r, s:s + ln], np.arange(g, g + ln))
+        # pads are exactly the tail after `valid`
+        assert np.array_equal(pad[g:g + ln], (np.arange(ln) >= valid).astype(np.uint8))
+        assert o.F[u] <= g and g + ln <= o.F[u] + o.S[u]
+    assert np.all(covered == 1)
+    # after the first segment of a slice, shard positions start 8-aligned
+    for i in range(1, len(segs)):
+        g0, s0, l0, _, r0, u0 = segs[i - 1]
+        g1, s1, l1, _, r1, u1 = segs[i]
+        if (r0, u0) == (r1, u1):
+            assert s1 == s0 + l0 and s1 % 8 == 0
+
+
+def test_named_workloads_layout(zlib, orc):
+    for fn, N in [(W.gpt2l_units, 8), (W.gpt_1p3b_units, 8), (W.llm_4b_units, 8), (W.finewrap_units, 16)]:
+        sizes = fn()
+        p = Z.ZeroPlan(sizes, N)
+        o = orc.Plan(sizes, N)
+        assert p.P_pad == o.P_pad and p.F == o.F.tolist() and p.Hoff == o.Hoff.tolist()
+        assert p.workspace is None
+        assert Z.zero_plan_workspace_bytes(p.handle) >= 40 * p.n_segments
+
+
+def test_bias_corrections_match_oracle_bitwise(zlib, orc):
+    for b1, b2 in [(0.9, 0.95), (0.9, 0.999), (0.8, 0.99), (0.5, 0.5)]:
+        for t in list(range(1, 3000)) + [10000, 123457, 2 ** 31 - 1]:
+            z = np.float32(Z.zero_bias_corrections(t, b1, b2))
+            o = orc.bias_corrections(t, b1, b2)
+            assert np.array_equal(np.array(z, np.float32).view(np.uint32), np.array(o, np.float32).view(np.uint32)), t
+
+
+def test_argument_errors_are_reported_on_the_host(zlib):
+    h = C.c_void_p()
+    sizes = (C.c_int64 * 2)(5, 7)
+    L = zlib
+    assert L.zero_plan_create(sizes, 2, 0, C.byref(h)) == B.ZERO_EINVAL
+    assert L.zero_plan_create(sizes, 2, 65, C.byref(h)) == B.ZERO_EINVAL
+    bad = (C.c_int64 * 2)(5, -1)
+    assert L.zero_plan_create(bad, 2, 2, C.byref(h)) == B.ZERO_EINVAL
+    assert L.zero_plan_create(None, 2, 2, C.byref(h)) == B.ZERO_EINVAL
+    assert L.zero_plan_create(sizes, 2, 2, None) == B.ZERO_EINVAL
+    huge = (C.c_int64 * 2)(2 ** 62, 2 ** 62)
+    assert L.zero_plan_create(huge, 2, 2, C.byref(h)) == B.ZERO_EINVAL
+    assert L.zero_plan_create(sizes, 2, 2, C.byref(h)) == B.ZERO_OK
+    # device calls on a plan without a workspace fail before any CUDA call
+    ptrs = (C.c_void_p * 2)(16, 32)
+    hp = B.AdamW().c()
+    assert L.zero_step(h, ptrs, B.ZERO_BF16, ptrs, ptrs, ptrs, None, None, B.ZERO_BF16, None, C.byref(hp), None, -1,
+                       None) == B.ZERO_ENOTATTACHED
+    assert L.zero_reduce_scatter(h, ptrs, B.ZERO_BF16, ptrs, C.c_float(1.0), None) == B.ZERO_ENOTATTACHED
+    assert L.zero_all_gather(h, ptrs, C.c_void_p(64), B.ZERO_BF16, -1, None) == B.ZERO_ENOTATTACHED
+    assert L.zero_grad_sqnorm(h, ptrs, B.ZERO_BF16, C.c_void_p(64), None) == B.ZERO_ENOTATTACHED
+    assert L.zero_plan_attach(h, None, 1 << 20, None) == B.ZERO_EINVAL
+    assert L.zero_plan_attach(h, C.c_void_p(1 << 12 | 8), 1 << 20, None) == B.ZERO_EALIGN
+    assert L.zero_plan_attach(h, C.c_void_p(1 << 12), 8, None) == B.ZERO_ENOMEM
+    assert L.zero_bias_corrections(0, C.c_float(0.9), C.c_float(0.95), C.byref(C.c_float()), C.byref(C.c_float())) \
+        == B.ZERO_EINVAL
+    assert L.zero_plan_query(None, None, None, None, None, None, None) == B.ZERO_EINVAL
+    for s in (0, -1, -2, -3, -4, -7, -99):
+        assert len(L.zero_status_string(s)) > 0
+    L.zero_plan_destroy(h)
+    L.zero_plan_destroy(None)
+
+
+def test_binding_refuses_wrong_tensors_on_the_host(zlib):
+    import torch
+    p = Z.ZeroPlan([10, 3], 2)  # host-only plan: device is None
+    with pytest.raises(ValueError):
+        Z.zero_reduce_scatter(p, torch.zeros(2, p.P_pad, dtype=torch.bfloat16),
+                              torch.zeros(2, p.H, dtype=torch.float32))

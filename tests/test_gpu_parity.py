@@ -1,0 +1,303 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Floating point is bit-exact (the method's arithmetic is fixed operation by
+operation; nothing is fused), integers exact.  The one quantity that is not
+bit-exact by construction is the binary64 sum of squares for the clip: the GPU
+adds per-segment partials in its own fixed order, so S is checked to a relative
+1e-12 of the oracle's exact sum, and the clip coefficient derived from it must
+then match bit for bit.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import fsdp_sharded_optimizer_step_gb300 as Z
+from fsdp_sharded_optimizer_step_gb300 import workloads as W
+from oracle import oracle as O
+from parity import SampledCase, SmallCase, aligned_copy, f32bits, host_bits, hp_for, oracle_grad_rows
+
+pytestmark = pytest.mark.gpu
+
+S_RTOL = 1e-12
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_ready():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from fsdp_sharded_optimizer_step_gb300 import build
+    build.build()
+    Z.lib()
+
+
+@pytest.fixture(autouse=True)
+def release_memory():
+    yield
+    import gc
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------ the pages' toy
+def test_toy_zero2_bit_exact_every_step():
+    """"ZeRO and FSDP sharding", Code: N=4, P=1000, w0=0, fp32 grads w - target_r,
+    50 steps, fp32 gather; every step equals unsharded AdamW bit for bit."""
+    dev = torch.device("cuda")
+    N, P, steps = 4, 1000, 50
+    plan = Z.ZeroPlan(W.toy_units(), N, dev)
+    targets = W.toy_targets(N, P, device=dev)
+    full = torch.zeros(P, dtype=torch.float32, device=dev)  # the gathered weights every rank sees
+    master, m, v = (Z.rank_buffers(N, plan.H, torch.float32, dev, zero=True) for _ in range(3))
+    grads = Z.rank_buffers(N, P, torch.float32, dev)
+    t_np = targets.cpu().numpy()
+    w_o = np.zeros(P, np.float32)
+    m_o = np.zeros(P, np.float32)
+    v_o = np.zeros(P, np.float32)
+    for t in range(1, steps + 1):
+        torch.sub(full.unsqueeze(0), targets, out=grads)  # each rank's local gradient of 1/2|w - target|^2
+        hp, ohp = hp_for(t)
+        Z.zero_step(plan, grads, master, m, v, hp, full=full)
+        g_o = [w_o - t_np[r] for r in range(N)]
+        O.adamw(g_o, O.F32, w_o, m_o, v_o, ohp, pdtype=O.F32)
+        assert np.array_equal(host_bits(full), f32bits(w_o)), f"step {t}"
+    ref = O.toy_unsharded(t_np, np.zeros(P, np.float32), steps, O.hparams())
+    assert np.array_equal(host_bits(full), f32bits(ref))
+    assert np.array_equal(host_bits(master).ravel(), f32bits(ref))
+
+
+# ------------------------------------------------------------------ small configs, every element
+SMALL = [
+    # (sizes, N, gdtype, pdtype)
+    ([1000], 4, W.F32, W.F32),
+    ([5, 0, 13, 1, 64, 257, 4099], 4, W.BF16, W.BF16),
+    ([70001, 3, 65537, 12345], 8, W.BF16, W.BF16),
+    ([70001, 3, 65537, 12345], 8, W.F32, W.BF16),
+    ([99991, 7, 40000], 3, W.BF16, W.F32),
+    ([33, 100003, 2, 77777], 5, W.F32, W.F32),
+    ([1, 2, 3, 4, 5, 6, 7, 8, 9, 131071], 16, W.BF16, W.BF16),
+    ([131072 * 3 + 5], 2, W.BF16, W.BF16),
+    ([4097, 1], 1, W.BF16, W.BF16),
+    ([300, 17, 9000], 64, W.BF16, W.BF16),
+    ([1000, 2000], 12, W.BF16, W.BF16),
+]
+
+
+@pytest.mark.parametrize("sizes,N,gd,pd", SMALL)
+def test_fused_step_bit_exact(sizes, N, gd, pd):
+    c = SmallCase(sizes, N, gd, pd, seed=len(sizes) * 31 + N)
+    for t in (1, 2, 3):
+        c.gpu_step(t)
+        assert c.oracle_step(t) == O.OK
+        c.assert_state_equal()
+        c.assert_full_equal()
+        c.assert_pshard_equal()
+
+
+def test_finewrap_shaped_small_bit_exact():
+    """Many small units at N=16 (log-uniform sizes): most slices have gradient
+    positions misaligned relative to their shard positions."""
+    sizes = W.finewrap_units(n_units=400, lo_log2=0, hi_log2=13, seed=4)
+    c = SmallCase(sizes, 16, W.BF16, W.BF16, seed=4)
+    segs = Z.zero_plan_segments(c.plan.handle)
+    assert sum(1 for s in segs if (s[0] - s[1]) % 8) > len(segs) // 2
+    for t in (1, 2):
+        c.gpu_step(t)
+        assert c.oracle_step(t) == O.OK
+        c.assert_state_equal()
+        c.assert_full_equal()
+
+
+def test_empty_and_degenerate_plans():
+    for sizes, N in (([], 4), ([0, 0], 3), ([1], 64), ([0, 1, 0], 2)):
+        c = SmallCase(sizes, N, W.BF16, W.BF16)
+        c.gpu_step(1)
+        assert c.oracle_step(1) == O.OK
+        if c.plan.P_pad:
+            c.assert_state_equal()
+            c.assert_full_equal()
+        torch.cuda.synchronize()
+
+
+def test_pads_stay_zero():
+    sizes = [13, 1, 250]
+    c = SmallCase(sizes, 8, W.BF16, W.BF16, state="zero")
+    pad = torch.from_numpy(c.pad.astype(bool))
+    mp = torch.from_numpy(c.map)
+    padpos = pad[mp].to(c.device)  # [N, H] mask of padding shard positions
+    c.master[padpos] = 0.0
+    for t in (1, 2, 3, 4):
+        c.gpu_step(t)
+    assert torch.all(c.master[padpos] == 0) and torch.all(c.m[padpos] == 0) and torch.all(c.v[padpos] == 0)
+    assert torch.all(c.full[torch.from_numpy(c.pad.astype(bool)).to(c.device)].float() == 0)
+
+
+def test_per_unit_launches_equal_one_multi_unit_launch():
+    sizes = [5000, 3, 70000, 1, 40961]
+    a = SmallCase(sizes, 8, W.BF16, W.BF16, seed=3)
+    b = SmallCase(sizes, 8, W.BF16, W.BF16, seed=3)
+    a.gpu_step(1)
+    for u in range(len(sizes)):
+        b.gpu_step(1, unit=u)
+    for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v), (a.full, b.full), (a.pshard, b.pshard)):
+        assert torch.equal(host_bits_t(x), host_bits_t(y))
+
+
+def host_bits_t(x):
+    return torch.from_numpy(host_bits(x).astype(np.int64))
+
+
+# ------------------------------------------------------------------ unfused parts
+def test_parts_compose_to_the_fused_step():
+    """reduce-scatter -> AdamW on the shard -> all-gather == the fused step, bit for bit;
+    each part also against the oracle."""
+    sizes = [70001, 3, 65537, 12345, 0, 9]
+    fused = SmallCase(sizes, 8, W.BF16, W.BF16, seed=9)
+    parts = SmallCase(sizes, 8, W.BF16, W.BF16, seed=9)
+    fused.gpu_step(1)
+    hp, _ = hp_for(1)
+    Z.zero_reduce_scatter(parts.plan, parts.grads, parts.gshard)
+    avg = O.avg_grad(parts.g_o, O.BF16, parts.pad)
+    assert np.array_equal(host_bits(parts.gshard), f32bits(avg)[parts.map])
+    Z.zero_adamw_shard_step(parts.plan, parts.gshard, parts.master, parts.m, parts.v, hp, pshard=parts.pshard)
+    Z.zero_all_gather_bf16(parts.plan, parts.pshard, parts.full)
+    for x, y in ((fused.master, parts.master), (fused.m, parts.m), (fused.v, parts.v), (fused.full, parts.full),
+                 (fused.pshard, parts.pshard)):
+        assert torch.equal(host_bits_t(x), host_bits_t(y))
+    assert fused.oracle_step(1) == O.OK
+    fused.assert_full_equal()
+
+
+def test_reduce_scatter_with_coefficient():
+    sizes = [1000, 77, 33333]
+    c = SmallCase(sizes, 4, W.F32, W.BF16, seed=2)
+    coef = np.float32(0.3711)
+    Z.zero_reduce_scatter(c.plan, c.grads, c.gshard, coef=float(coef))
+    avg = O.avg_grad(c.g_o, O.F32, c.pad)
+    want = (avg * coef).astype(np.float32)  # one binary32 multiply per element
+    assert np.array_equal(host_bits(c.gshard), f32bits(want)[c.map])
+
+
+def test_all_gather_per_unit_and_fp32():
+    sizes = [1001, 5, 20000, 3]
+    for pd in (W.BF16, W.F32):
+        c = SmallCase(sizes, 4, W.BF16, pd, seed=5)
+        g = torch.Generator().manual_seed(1)
+        src = aligned_copy(torch.randn(4, c.plan.H, generator=g).to(c.pshard.dtype), c.device)
+        ref = src.cpu().numpy() if pd == W.F32 else None
+        full = torch.zeros_like(c.full)
+        for u in range(len(sizes)):
+            Z.zero_all_gather(c.plan, src, full, unit=u)
+        want = np.zeros(c.plan.P_pad, dtype=np.uint32 if pd == W.F32 else np.uint16)
+        want[c.map.ravel()] = host_bits(src).ravel()
+        assert np.array_equal(host_bits(full), want)
+        if ref is not None:
+            assert np.array_equal(full.cpu().numpy()[c.map], ref)
+
+
+def test_grad_sqnorm_close_to_exact_and_deterministic():
+    sizes = [70001, 3, 65537, 12345, 9]
+    c = SmallCase(sizes, 8, W.BF16, W.BF16, seed=11, outlier_frac=1e-3, outlier_scale=100.0)
+    out = torch.zeros(1, dtype=torch.float64, device=c.device)
+    Z.zero_grad_sqnorm(c.plan, c.grads, out)
+    S1 = out.item()
+    Z.zero_grad_sqnorm(c.plan, c.grads, out)
+    assert out.item() == S1  # fixed reduction order: same bits every run
+    S_o = O.sqnorm(c.g_o, O.BF16, c.pad)
+    assert abs(S1 - S_o) <= S_RTOL * S_o
+
+
+# ------------------------------------------------------------------ clipping
+@pytest.mark.parametrize("max_norm", [1e-4, 1.0, 1e6])
+def test_clipped_step_bit_exact(max_norm):
+    sizes = [70001, 3, 65537, 12345, 9]
+    c = SmallCase(sizes, 8, W.BF16, W.BF16, seed=12, grad_sigma=1e-2, outlier_frac=1e-3, outlier_scale=100.0)
+    for t in (1, 2):
+        c.gpu_step(t, max_norm=max_norm)
+        assert c.oracle_step(t, max_norm=max_norm) == O.OK
+        S_gpu = c.sq.item()
+        assert abs(S_gpu - c.S_o) <= S_RTOL * c.S_o
+        assert O.clip_coef(S_gpu, max_norm) == O.clip_coef(c.S_o, max_norm)
+        c.assert_state_equal()
+        c.assert_full_equal()
+        c.assert_pshard_equal()
+        avg = O.avg_grad(c.g_o, O.BF16, c.pad)
+        assert np.array_equal(host_bits(c.gshard), f32bits(avg)[c.map])  # the unclipped averaged shard
+
+
+def test_clipped_step_skipped_when_norm_not_finite():
+    sizes = [1000, 3000]
+    c = SmallCase(sizes, 4, W.BF16, W.BF16, seed=13)
+    c.grads[2, 17] = float("inf")
+    before = [x.clone() for x in (c.master, c.m, c.v, c.full, c.pshard)]
+    c.gpu_step(1, max_norm=1.0)
+    assert math.isinf(c.sq.item())
+    for x, y in zip(before, (c.master, c.m, c.v, c.full, c.pshard)):
+        assert torch.equal(host_bits_t(x), host_bits_t(y))
+    c.g_o = oracle_grad_rows(c.grads)
+    assert c.oracle_step(1, max_norm=1.0) == O.ENONFINITE
+
+
+def test_nan_and_inf_without_clip_follow_ieee():
+    sizes = [4096]
+    c = SmallCase(sizes, 4, W.F32, W.BF16, seed=14)
+    c.grads[1, 5] = float("nan")
+    c.grads[0, 9] = float("inf")
+    c.grads[3, 9] = float("-inf")
+    c.grads[2, 11] = float("inf")
+    c.g_o = oracle_grad_rows(c.grads)
+    c.gpu_step(1)
+    assert c.oracle_step(1) == O.OK
+    c.assert_state_equal()
+    c.assert_full_equal()
+
+
+def test_runs_on_a_side_stream():
+    c = SmallCase([70001, 5], 8, W.BF16, W.BF16, seed=15)
+    s = torch.cuda.Stream()
+    hp, _ = hp_for(1)
+    with torch.cuda.stream(s):
+        Z.zero_step(c.plan, c.grads, c.master, c.m, c.v, hp, full=c.full, stream=s)
+    s.synchronize()
+    assert c.oracle_step(1) == O.OK
+    c.assert_full_equal()
+
+
+# ------------------------------------------------------------------ full-size workloads (sampled)
+@pytest.mark.slow
+def test_gpt2l_zero1_full_size_sampled():
+    c = SampledCase("gpt2l", n_random=300000, extra_units=(37,))
+    for t in (1, 2):
+        c.gpu_step(t)
+        out = c.oracle_step(t)
+        c.assert_sample_equal(out)
+
+
+@pytest.mark.slow
+def test_1p3b_zero2_clip_full_size():
+    c = SampledCase("1p3b_clip", n_random=200000)
+    S = c.oracle_sqnorm()
+    coef = O.clip_coef(S, 1.0)
+    assert coef < 1.0  # the outliers make the norm exceed 1: clipping is active
+    for t in (1, 2):
+        c.gpu_step(t)
+        S_gpu = c.sq.item()
+        assert abs(S_gpu - S) <= S_RTOL * S
+        assert O.clip_coef(S_gpu, 1.0) == coef
+        out = c.oracle_step(t, coef=coef)
+        c.assert_sample_equal(out)
+
+
+@pytest.mark.slow
+def test_finewrap_full_size_sampled():
+    c = SampledCase("finewrap", n_random=200000, extra_units=(0, 1, 2, 4095))
+    c.gpu_step(1)
+    c.assert_sample_equal(c.oracle_step(1))
+
+
+@pytest.mark.slow
+def test_4b_zero3_full_size_sampled():
+    c = SampledCase("4b_z3", n_random=200000, extra_units=(32,))
+    c.gpu_step(1)
+    c.assert_sample_equal(c.oracle_step(1))
