@@ -176,7 +176,10 @@ class ZeroPlan:
         self.device = None
         self.workspace = None
         if device is not None:
-            self.device = torch.device(device)
+            device = torch.device(device)
+            if device.type == "cuda" and device.index is None:
+                device = torch.device("cuda", torch.cuda.current_device())
+            self.device = device
             nbytes = zero_plan_workspace_bytes(self.handle)
             self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
             zero_plan_attach(self.handle, self.workspace, stream)

@@ -75,6 +75,10 @@ CONFIGS = {
     "finewrap": dict(desc="fine-wrap stress: N=16, 4096 log-uniform units in [2^10, 2^22), bf16 grads N(0,1e-3)",
                      units=finewrap_units, N=16, gdtype=BF16, pdtype=BF16, stage=2, steps=3, max_norm=0.0,
                      grad_sigma=1e-3, master_sigma=0.02),
+    "gpt2l_prof": dict(desc="profiling case: the first two GPT-2-Large units (token embedding + one block, "
+                            "84,006,400 params), N=8, bf16 grads N(0,1e-3); 3.5 GB of traffic per step",
+                       units=lambda: gpt2l_units()[:2], N=8, gdtype=BF16, pdtype=BF16, stage=1, steps=3, max_norm=0.0,
+                       grad_sigma=1e-3, master_sigma=0.02),
     "4b_z3": dict(desc="4B ZeRO-3: N=8, 33 units, bf16 grads N(0,1e-3), per-unit bf16 all-gather",
                   units=llm_4b_units, N=8, gdtype=BF16, pdtype=BF16, stage=3, steps=3, max_norm=0.0,
                   grad_sigma=1e-3, master_sigma=0.02),
