@@ -15,7 +15,7 @@ import torch
 
 from . import build as _build
 
-ZERO_OK, ZERO_EINVAL, ZERO_ENOMEM, ZERO_ECUDA, ZERO_EALIGN, ZERO_ENOTATTACHED = 0, -1, -2, -3, -4, -7
+ZERO_OK, ZERO_EINVAL, ZERO_ENOMEM, ZERO_ECUDA, ZERO_EALIGN, ZERO_ENOTATTACHED, ZERO_ERANGE = 0, -1, -2, -3, -4, -7, -8
 ZERO_F32, ZERO_BF16 = 0, 1
 ZERO_MAX_RANKS = 64
 
@@ -81,6 +81,7 @@ def lib():
             "zero_all_gather": (C.c_int, [p, pp, p, i32, i32, p]),
             "zero_all_gather_bf16": (C.c_int, [p, pp, p, i32, p]),
             "zero_step": (C.c_int, [p, pp, i32, pp, pp, pp, p, pp, i32, pp, p, p, i32, p]),
+            "zero_grad_sqnorm_noalloc": (C.c_int, [pp, i32, i32, i64, p, p]),
             "zero_status_string": (C.c_char_p, [C.c_int]),
             "zero_last_cuda_error": (C.c_int, []),
         }
@@ -304,3 +305,21 @@ def zero_step(plan, grads, master, m, v, hp: AdamW, full=None, pshard=None, gsha
     c = hp.c()
     _check(lib().zero_step(plan.handle, g, gd, W, M, V, fp, ps, pdt, gs, C.byref(c), sq, int(unit),
                            _stream(stream, plan.device)), "zero_step")
+
+
+def zero_grad_sqnorm_noalloc(grads, sqnorm_out, stream=None):
+    """Sum of squares of the averaged gradient over flat rank buffers, with no
+    device allocation (see include/zero.h); padding entries must hold 0."""
+    rows = list(grads.unbind(0)) if isinstance(grads, torch.Tensor) else list(grads)
+    n = rows[0].numel()
+    dev = rows[0].device
+    for r in rows:
+        if r.device != dev or r.dtype != rows[0].dtype or r.dim() != 1 or not r.is_contiguous() or r.numel() != n:
+            raise ValueError("grads: rank buffers must be contiguous 1-D tensors of one dtype, length and device")
+    if rows[0].dtype not in _DTYPES:
+        raise ValueError(f"grads: dtype {rows[0].dtype} not allowed")
+    if sqnorm_out.device != dev or sqnorm_out.dtype != torch.float64:
+        raise ValueError("sqnorm_out: need a float64 tensor on the gradients' device")
+    arr = (C.c_void_p * len(rows))(*[r.data_ptr() for r in rows])
+    _check(lib().zero_grad_sqnorm_noalloc(arr, len(rows), _DTYPES[rows[0].dtype], n, C.c_void_p(sqnorm_out.data_ptr()),
+                                          _stream(stream, dev)), "zero_grad_sqnorm_noalloc")

@@ -187,6 +187,7 @@ extern "C" const char *zero_status_string(int status) {
         case ZERO_ECUDA: return "CUDA runtime error";
         case ZERO_EALIGN: return "device pointer not 16-byte aligned";
         case ZERO_ENOTATTACHED: return "plan has no device workspace (call zero_plan_attach)";
+        case ZERO_ERANGE: return "size beyond the fixed capacity of the allocation-free entry point";
         default: return "unknown status";
     }
 }

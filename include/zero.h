@@ -81,7 +81,8 @@ enum {
     ZERO_ENOMEM = -2,      /* host allocation failed, or the workspace is too small */
     ZERO_ECUDA = -3,       /* a CUDA runtime call failed (launch, copy, device query) */
     ZERO_EALIGN = -4,      /* a device pointer is not 16-byte aligned */
-    ZERO_ENOTATTACHED = -7 /* the plan has no device workspace yet (zero_plan_attach) */
+    ZERO_ENOTATTACHED = -7, /* the plan has no device workspace yet (zero_plan_attach) */
+    ZERO_ERANGE = -8        /* a size beyond a fixed capacity (zero_grad_sqnorm_noalloc) */
 };
 
 enum { ZERO_F32 = 0, ZERO_BF16 = 1 };
@@ -212,6 +213,39 @@ int zero_step(const zero_plan *plan, const void *const *grads, int32_t gdtype, f
               float *const *m, float *const *v, void *full, void *const *pshard, int32_t pdtype,
               float *const *gshard_ws, const zero_hparams *hp, double *sqnorm_dev, int32_t unit,
               zero_stream_t stream);
+
+/* ---------------------------------------------------------------- without allocation */
+
+/* No counterpart on the pages: an addition for callers that cannot allocate
+ * device memory.  A gradient-norm check often has to run exactly when memory
+ * is exhausted (logging the norm of a step that ran out of memory, a watchdog
+ * for non-finite gradients inside a framework whose caching allocator holds
+ * nearly all of the GPU); there a cudaMalloc, or a request to the framework's
+ * allocator, fails or makes the allocator release and re-reserve memory.
+ *
+ * Computes the same quantity as zero_grad_sqnorm -- S = sum of g^2, g the
+ * rank-ordered binary32 average of the N gradients, each square exact in
+ * binary64, partials added in a fixed order -- over n flat positions, with no
+ * plan and no workspace: every position counts, so padding entries must hold
+ * 0 (as a flat-parameter layout keeps them).  It allocates nothing: the
+ * per-chunk partial sums live in one array of ZERO_NOALLOC_MAX_CHUNKS binary64
+ * values (256 KB) compiled into the library, which every GPU that loads the
+ * library holds until the process exits.
+ *   grads     [n_ranks] device pointers to n elements of gdtype each (aligned
+ *             to the element size).
+ *   n         0 <= n <= ZERO_NOALLOC_MAX_CHUNKS * ZERO_NOALLOC_CHUNK
+ *             (2^32 elements); larger n returns ZERO_ERANGE before any launch.
+ *   sqnorm_dev  DEVICE binary64 receiving S (8-byte aligned), asynchronously.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  All calls share the one array (it keeps the last call's
+ * partials, and every call overwrites the ones it reads), so calls whose work
+ * overlaps on the GPU -- on two streams, or from two threads -- race; order them
+ * on one stream. */
+#define ZERO_NOALLOC_CHUNK 131072
+#define ZERO_NOALLOC_MAX_CHUNKS 32768
+int zero_grad_sqnorm_noalloc(const void *const *grads, int32_t n_ranks, int32_t gdtype, int64_t n,
+                             double *sqnorm_dev, zero_stream_t stream);
 
 /* ---------------------------------------------------------------- diagnostics */
 
