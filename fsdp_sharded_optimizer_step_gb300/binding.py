@@ -82,6 +82,7 @@ def lib():
             "zero_all_gather_bf16": (C.c_int, [p, pp, p, i32, p]),
             "zero_step": (C.c_int, [p, pp, i32, pp, pp, pp, p, pp, i32, pp, p, p, i32, p]),
             "zero_grad_sqnorm_noalloc": (C.c_int, [pp, i32, i32, i64, p, p]),
+            "zero_plan_device_errors": (C.c_int, [p, p, p]),
             "zero_status_string": (C.c_char_p, [C.c_int]),
             "zero_last_cuda_error": (C.c_int, []),
         }
@@ -152,6 +153,14 @@ def zero_plan_workspace_bytes(handle):
 def zero_plan_attach(handle, workspace: torch.Tensor, stream=None):
     _check(lib().zero_plan_attach(handle, C.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
                                   _stream(stream, workspace.device)), "zero_plan_attach")
+
+
+def zero_plan_device_errors(plan, stream=None):
+    """Reads and clears the plan's device error word (0: every bounded wait completed)."""
+    e = C.c_int32()
+    _check(lib().zero_plan_device_errors(plan.handle, _stream(stream, plan.device), C.byref(e)),
+           "zero_plan_device_errors")
+    return e.value
 
 
 def zero_bias_corrections(t, b1=0.9, b2=0.95):

@@ -52,6 +52,7 @@ struct zero_plan {
     double *d_partials = nullptr;   // one binary64 partial sum per segment
     double *d_sqnorm = nullptr;     // S of the last clipped step
     float *d_coef = nullptr;        // clip coefficient of the last clipped step
+    int *d_err = nullptr;           // device error word: non-zero after a bounded wait expired
 };
 
 namespace zero {

@@ -22,6 +22,11 @@
 namespace zero {
 
 constexpr int kThreads = 256;
+#ifndef ZERO_PIPE_CONSUMER_WARPS
+#define ZERO_PIPE_CONSUMER_WARPS 16
+#endif
+constexpr int kConsumerWarps = ZERO_PIPE_CONSUMER_WARPS;
+constexpr int kPipeThreads = (kConsumerWarps + 1) * 32;
 
 struct KParams {
     const Seg *segs;
@@ -34,6 +39,9 @@ struct KParams {
     float coef;             // host clip coefficient (reduce-scatter); 1 = none
     int32_t write_g, want_partials, use_coef_dev;
     double *partials;       // per segment, indexed by absolute segment number
+    int *err;               // device error word (a bounded wait expired)
+    int32_t tile, stages;   // pipeline geometry of k_fused_pipe
+    int64_t p_pad, h_len;   // element counts of full-length and shard buffers (diagnostic bounds checks)
     const float *coef_dev;  // device clip coefficient (NaN: skip the step)
     void *full;
     const void *grads[ZERO_MAX_RANKS];
@@ -43,6 +51,23 @@ struct KParams {
     void *pshard[ZERO_MAX_RANKS];
     float *gshard[ZERO_MAX_RANKS];
 };
+
+// Diagnostic build (-DZERO_SELFCHECK): every shared/global access of the
+// pipeline is checked against its buffer and alignment first; a failed check
+// records its code in *err and the access is skipped.
+#ifdef ZERO_SELFCHECK
+__device__ __forceinline__ bool guard_ok(bool ok, int code, int *err) {
+    if (!ok) atomicCAS(err, 0, code);
+    return ok;
+}
+#define ZERO_GUARD(cond, code) guard_ok((cond), (code), p.err)
+#else
+#define ZERO_GUARD(cond, code) true
+#endif
+
+__device__ __forceinline__ bool aligned_to(const void *ptr, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0;
+}
 
 // ------------------------------------------------------------------ element math
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
@@ -228,41 +253,50 @@ __device__ __forceinline__ SegSplit split_segment(const Seg &sg) {
 
 // ------------------------------------------------------------------ fused step
 // reduce-scatter + average + AdamW + cast + all-gather, one pass.
+
+// Direct (register) path for one segment, spread over nthr threads: the
+// 8-wide groups of [k0, tail0) when `body` is set, and always the head and
+// tail elements.
 template <int GD, int NR>
-__global__ void __launch_bounds__(kThreads, 2) k_fused_step(const KParams p) {
-    const Seg sg = p.segs[p.seg_base + blockIdx.x];
-    const SegSplit sp = split_segment(sg);
+__device__ __forceinline__ void fused_direct(const KParams &p, const Seg &sg, const SegSplit &sp, int tid, int nthr,
+                                             bool body) {
     const int r = sg.rank;
     float *__restrict__ W = p.master[r] + sg.s_off;
     float *__restrict__ M = p.m[r] + sg.s_off;
     float *__restrict__ V = p.v[r] + sg.s_off;
     void *full = p.full;
     void *ps = p.pshard[r];
-
-    for (int i = threadIdx.x; i < sp.ngroups; i += kThreads) {
-        const int k = sp.k0 + 8 * i;
-        float acc[8], w[8], m[8], v[8];
-        fold8<GD, NR>(p, sg.g_off + k, sp.gvec, acc);
-        load8(W + k, w);
-        load8(M + k, m);
-        load8(V + k, v);
-        if (k + 8 > sg.valid) {
+    if (body) {
+        for (int i = tid; i < sp.ngroups; i += nthr) {
+            const int k = sp.k0 + 8 * i;
+            if (!ZERO_GUARD(k + 8 <= sg.len && sg.s_off + k + 8 <= p.h_len && sg.g_off + k + 8 <= p.p_pad &&
+                                aligned_to(W + k, 16),
+                            30))
+                continue;
+            float acc[8], w[8], m[8], v[8];
+            fold8<GD, NR>(p, sg.g_off + k, sp.gvec, acc);
+            load8(W + k, w);
+            load8(M + k, m);
+            load8(V + k, v);
+            if (k + 8 > sg.valid) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                if (k + e >= sg.valid) acc[e] = 0.0f;
+                for (int e = 0; e < 8; ++e)
+                    if (k + e >= sg.valid) acc[e] = 0.0f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) adamw(average(acc[e], p), w[e], m[e], v[e], p.c);
+            store8(W + k, w);
+            store8(M + k, m);
+            store8(V + k, v);
+            if (full != nullptr) store_param8(full, sg.g_off + k, p.pdtype, sp.gvec, w);
+            if (ps != nullptr) store_param8(ps, sg.s_off + k, p.pdtype, true, w);
         }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) adamw(average(acc[e], p), w[e], m[e], v[e], p.c);
-        store8(W + k, w);
-        store8(M + k, m);
-        store8(V + k, v);
-        if (full != nullptr) store_param8(full, sg.g_off + k, p.pdtype, sp.gvec, w);
-        if (ps != nullptr) store_param8(ps, sg.s_off + k, p.pdtype, true, w);
     }
     // head and tail, one element per thread
     const int nedge = sp.k0 + (sg.len - sp.tail0);
-    for (int t = threadIdx.x; t < nedge; t += kThreads) {
+    for (int t = tid; t < nedge; t += nthr) {
         const int k = t < sp.k0 ? t : sp.tail0 + (t - sp.k0);
+        if (!ZERO_GUARD(k >= 0 && k < sg.len && sg.s_off + k < p.h_len && sg.g_off + k < p.p_pad, 31)) continue;
         float acc = fold1<GD, NR>(p, sg.g_off + k);
         if (k >= sg.valid) acc = 0.0f;
         float w = W[k], m = M[k], v = V[k];
@@ -272,6 +306,286 @@ __global__ void __launch_bounds__(kThreads, 2) k_fused_step(const KParams p) {
         V[k] = v;
         if (full != nullptr) store_param1(full, sg.g_off + k, p.pdtype, w);
         if (ps != nullptr) store_param1(ps, sg.s_off + k, p.pdtype, w);
+    }
+}
+
+// ------------------------------------------------------------------ fused step, bulk-copy pipeline
+// Persistent, warp-specialised: CTA b takes segments b, b + gridDim.x, ...
+// One producer thread streams each aligned segment body, tile by tile, into a
+// ring of `stages` shared-memory buffers with 1-D bulk copies (cp.async.bulk,
+// completion counted in bytes on a per-stage mbarrier): the N gradient rows
+// and master/m/v of `tile` elements.  The consumer warps wait for a stage,
+// compute from shared memory, store master/m/v and the params straight to
+// global memory, and release the stage.  Copies stay in flight while the
+// consumers compute, which the register-only kernel cannot do.  Heads, tails
+// and segments whose gradient positions are not aligned like their shard
+// positions take the direct path in the consumer warps.
+//
+// Every wait is bounded (kWaitLimitNs of %globaltimer): on expiry the waiting
+// thread records the failure in *p.err, stops issuing work, and the producer
+// waits (again bounded) for the copies it already issued before the CTA exits.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *ptr) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits until the phase of `bar` with the given parity has completed, for at
+// most kWaitLimitNs; false on expiry.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar,
+                                          uint64_t policy) {
+#ifdef ZERO_PIPE_EVICT_FIRST
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst_smem)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+#else
+    (void)policy;
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst_smem)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+#endif
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol = 0;
+#ifdef ZERO_PIPE_EVICT_FIRST
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+#endif
+    return pol;
+}
+
+// Stage layout: N gradient rows of `tile` elements, then master, m, v.
+struct StageLayout {
+    uint32_t grad_row_bytes, state_off, bytes;
+};
+
+__device__ __forceinline__ StageLayout stage_layout(int n_ranks, int gbytes, int tile) {
+    StageLayout L;
+    L.grad_row_bytes = static_cast<uint32_t>(tile * gbytes);
+    L.state_off = L.grad_row_bytes * n_ranks;
+    L.bytes = L.state_off + 3u * static_cast<uint32_t>(tile) * 4u;
+    return L;
+}
+
+template <int GD, int NR>
+__global__ void __launch_bounds__(kPipeThreads, 1) k_fused_pipe(const KParams p, int64_t nseg) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int GB = GD == ZERO_BF16 ? 2 : 4;
+    const int n = NR > 0 ? NR : p.n_ranks;
+    const int tile = p.tile, stages = p.stages;
+    const StageLayout L = stage_layout(n, GB, tile);
+    uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(stages) * L.bytes);
+    uint64_t *empty_bar = full_bar + stages;
+    __shared__ int abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], kConsumerWarps);
+        }
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ---------------- producer
+        if (lane != 0) return;
+        const uint64_t pol = evict_first_policy();
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_mask = 0, issued_parity = 0;  // per stage: copies issued at least once, parity of the last
+        bool ok = true;
+        for (int64_t si = blockIdx.x; si < nseg && ok; si += gridDim.x) {
+            const Seg sg = p.segs[p.seg_base + si];
+            const SegSplit sp = split_segment(sg);
+            if (!sp.gvec) continue;
+            const int r = sg.rank;
+            for (int k = sp.k0; k < sp.tail0; k += tile) {
+                const int len = min(tile, sp.tail0 - k);
+                if (!mbar_wait(&empty_bar[stage], phase ^ 1u) || *reinterpret_cast<volatile int *>(&abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                unsigned char *buf = smem + static_cast<size_t>(stage) * L.bytes;
+                const uint32_t gbytes = static_cast<uint32_t>(len * GB), sbytes = static_cast<uint32_t>(len * 4);
+                if (!ZERO_GUARD(len > 0 && len <= tile && (gbytes & 15u) == 0 && sg.g_off + k + len <= p.p_pad &&
+                                    sg.s_off + k + len <= p.h_len && r >= 0 && r < n && stage >= 0 && stage < stages,
+                                10)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full_bar[stage], gbytes * n + 3u * sbytes);
+                for (int q = 0; q < n; ++q) {
+                    const unsigned char *src = static_cast<const unsigned char *>(p.grads[q]) + (sg.g_off + k) * GB;
+                    if (ZERO_GUARD(aligned_to(src, 16) && aligned_to(buf + q * L.grad_row_bytes, 16), 11))
+                        bulk_load(buf + q * L.grad_row_bytes, src, gbytes, &full_bar[stage], pol);
+                }
+                unsigned char *st = buf + L.state_off;
+                if (ZERO_GUARD(aligned_to(p.master[r] + sg.s_off + k, 16) && aligned_to(p.m[r] + sg.s_off + k, 16) &&
+                                   aligned_to(p.v[r] + sg.s_off + k, 16) && aligned_to(st, 16) &&
+                                   L.state_off + 3u * static_cast<uint32_t>(tile) * 4u <= L.bytes,
+                               12)) {
+                    bulk_load(st, p.master[r] + sg.s_off + k, sbytes, &full_bar[stage], pol);
+                    bulk_load(st + tile * 4, p.m[r] + sg.s_off + k, sbytes, &full_bar[stage], pol);
+                    bulk_load(st + 2 * tile * 4, p.v[r] + sg.s_off + k, sbytes, &full_bar[stage], pol);
+                }
+                issued_mask |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            atomicExch(p.err, 1);
+            abort_flag = 1;
+            // drain: wait (bounded) for the last copies issued into each stage
+            for (int s = 0; s < stages; ++s)
+                if (issued_mask & (1u << s)) mbar_wait(&full_bar[s], (issued_parity >> s) & 1u);
+        }
+        return;
+    }
+
+    // ---------------- consumers: every consumer warp takes every tile, so each
+    // stage's mbarrier phases are always waited on in order by the same warps
+    // (a stage shared between consumer sets that alternate would let a waiter
+    // for phase k pass while the barrier is still in phase k-1: the parity of
+    // phase k then reads as already complete).
+    const int ct = threadIdx.x;  // 0 .. kConsumerWarps*32 - 1
+    constexpr int CT = kConsumerWarps * 32;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int64_t si = blockIdx.x; si < nseg; si += gridDim.x) {
+        const Seg sg = p.segs[p.seg_base + si];
+        const SegSplit sp = split_segment(sg);
+        fused_direct<GD, NR>(p, sg, sp, ct, CT, !sp.gvec);
+        if (!sp.gvec) continue;
+        const int r = sg.rank;
+        float *__restrict__ Wg = p.master[r] + sg.s_off;
+        float *__restrict__ Mg = p.m[r] + sg.s_off;
+        float *__restrict__ Vg = p.v[r] + sg.s_off;
+        void *full = p.full;
+        void *ps = p.pshard[r];
+        for (int k = sp.k0; k < sp.tail0; k += tile) {
+            const int len = min(tile, sp.tail0 - k);
+            if (!mbar_wait(&full_bar[stage], phase) || *reinterpret_cast<volatile int *>(&abort_flag)) {
+                if (lane == 0) atomicExch(p.err, 2);
+                abort_flag = 1;
+                return;
+            }
+            const unsigned char *buf = smem + static_cast<size_t>(stage) * L.bytes;
+            const float *Ws = reinterpret_cast<const float *>(buf + L.state_off);
+            const float *Ms = Ws + tile;
+            const float *Vs = Ms + tile;
+            for (int e = 4 * ct; e < len; e += 4 * CT) {
+                if (!ZERO_GUARD(e + 4 <= tile && sg.s_off + k + e + 4 <= p.h_len && sg.g_off + k + e + 4 <= p.p_pad &&
+                                    aligned_to(Wg + k + e, 16) && aligned_to(Ws + e, 16) &&
+                                    (full == nullptr || aligned_to(static_cast<unsigned char *>(full) + (sg.g_off + k + e) * (p.pdtype == ZERO_BF16 ? 2 : 4), p.pdtype == ZERO_BF16 ? 8 : 16)),
+                                20))
+                    continue;
+                float acc[4];
+                if constexpr (GD == ZERO_BF16) {
+                    const uint2 x0 = *reinterpret_cast<const uint2 *>(buf + e * 2);
+                    acc[0] = __uint_as_float(x0.x << 16); acc[1] = __uint_as_float(x0.x & 0xFFFF0000u);
+                    acc[2] = __uint_as_float(x0.y << 16); acc[3] = __uint_as_float(x0.y & 0xFFFF0000u);
+#pragma unroll
+                    for (int q = 1; q < (NR > 0 ? NR : ZERO_MAX_RANKS); ++q) {
+                        if (NR == 0 && q >= n) break;
+                        const uint2 x = *reinterpret_cast<const uint2 *>(buf + q * L.grad_row_bytes + e * 2);
+                        acc[0] = __fadd_rn(acc[0], __uint_as_float(x.x << 16));
+                        acc[1] = __fadd_rn(acc[1], __uint_as_float(x.x & 0xFFFF0000u));
+                        acc[2] = __fadd_rn(acc[2], __uint_as_float(x.y << 16));
+                        acc[3] = __fadd_rn(acc[3], __uint_as_float(x.y & 0xFFFF0000u));
+                    }
+                } else {
+                    const float4 x0 = *reinterpret_cast<const float4 *>(buf + e * 4);
+                    acc[0] = x0.x; acc[1] = x0.y; acc[2] = x0.z; acc[3] = x0.w;
+#pragma unroll
+                    for (int q = 1; q < (NR > 0 ? NR : ZERO_MAX_RANKS); ++q) {
+                        if (NR == 0 && q >= n) break;
+                        const float4 x = *reinterpret_cast<const float4 *>(buf + q * L.grad_row_bytes + e * 4);
+                        acc[0] = __fadd_rn(acc[0], x.x);
+                        acc[1] = __fadd_rn(acc[1], x.y);
+                        acc[2] = __fadd_rn(acc[2], x.z);
+                        acc[3] = __fadd_rn(acc[3], x.w);
+                    }
+                }
+                const float4 w4 = *reinterpret_cast<const float4 *>(Ws + e);
+                const float4 m4 = *reinterpret_cast<const float4 *>(Ms + e);
+                const float4 v4 = *reinterpret_cast<const float4 *>(Vs + e);
+                float w[4] = {w4.x, w4.y, w4.z, w4.w}, m[4] = {m4.x, m4.y, m4.z, m4.w}, v[4] = {v4.x, v4.y, v4.z, v4.w};
+                const int kk = k + e;
+                if (kk + 4 > sg.valid) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (kk + i >= sg.valid) acc[i] = 0.0f;
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) adamw(average(acc[i], p), w[i], m[i], v[i], p.c);
+                __stcs(reinterpret_cast<float4 *>(Wg + kk), make_float4(w[0], w[1], w[2], w[3]));
+                __stcs(reinterpret_cast<float4 *>(Mg + kk), make_float4(m[0], m[1], m[2], m[3]));
+                __stcs(reinterpret_cast<float4 *>(Vg + kk), make_float4(v[0], v[1], v[2], v[3]));
+                if (p.pdtype == ZERO_BF16) {
+                    const uint2 h = make_uint2(f32_to_bf16_rne(w[0]) | (f32_to_bf16_rne(w[1]) << 16),
+                                               f32_to_bf16_rne(w[2]) | (f32_to_bf16_rne(w[3]) << 16));
+                    if (full != nullptr) __stcs(reinterpret_cast<uint2 *>(static_cast<unsigned short *>(full) + sg.g_off + kk), h);
+                    if (ps != nullptr) __stcs(reinterpret_cast<uint2 *>(static_cast<unsigned short *>(ps) + sg.s_off + kk), h);
+                } else {
+                    const float4 f = make_float4(w[0], w[1], w[2], w[3]);
+                    if (full != nullptr) __stcs(reinterpret_cast<float4 *>(static_cast<float *>(full) + sg.g_off + kk), f);
+                    if (ps != nullptr) __stcs(reinterpret_cast<float4 *>(static_cast<float *>(ps) + sg.s_off + kk), f);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[stage]);
+            if (++stage == stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
     }
 }
 
@@ -494,6 +808,9 @@ static void fill_common(const zero_plan *plan, KParams &kp) {
     kp.inv_n = kp.pow2 ? 1.0f / static_cast<float>(n) : 0.0f;  // exact for a power of two
     kp.coef = 1.0f;
     kp.partials = plan->d_partials;
+    kp.err = plan->d_err;
+    kp.p_pad = plan->p_pad;
+    kp.h_len = plan->H;
 }
 
 static int launch_status() {
@@ -539,10 +856,97 @@ static int seg_range(const zero_plan *plan, int32_t unit, int64_t &begin, int64_
         }                                                                                            \
     }
 
-ZERO_KERNEL_DISPATCH(k_fused_step)
 ZERO_KERNEL_DISPATCH(k_reduce)
 
 static bool valid_dtype(int32_t d) { return d == ZERO_BF16 || d == ZERO_F32; }
+
+// ------------------------------------------------------------------ pipeline geometry and launch
+#ifndef ZERO_PIPE_SMEM_BUDGET
+#define ZERO_PIPE_SMEM_BUDGET (200 * 1024)
+#endif
+#ifndef ZERO_PIPE_STAGE_TARGET
+#define ZERO_PIPE_STAGE_TARGET (64 * 1024)
+#endif
+constexpr int kMaxStages = 16;
+
+struct PipeGeometry {
+    int tile, stages;
+    size_t smem;
+};
+
+// Tile: a multiple of the consumers' pass width (4 elements per consumer
+// thread) close to ZERO_PIPE_STAGE_TARGET bytes per stage (N gradient rows +
+// master/m/v), halved while two stages would not fit the shared-memory
+// budget; then as many stages as fit the budget.
+static PipeGeometry pipe_geometry(int n_ranks, int gdtype) {
+    const int gb = gdtype == ZERO_BF16 ? 2 : 4;
+    const size_t per_elem = static_cast<size_t>(n_ranks) * gb + 12;
+    const size_t quantum = 4 * kConsumerWarps * 32;
+    size_t mult = ZERO_PIPE_STAGE_TARGET / (quantum * per_elem);
+    size_t tile = quantum * (mult > 0 ? mult : 1);
+    while (tile > 64 && 2 * tile * per_elem > ZERO_PIPE_SMEM_BUDGET) tile >>= 1;
+    const size_t stage_bytes = tile * per_elem;
+    int stages = static_cast<int>(ZERO_PIPE_SMEM_BUDGET / stage_bytes);
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2) stages = 2;
+    PipeGeometry g;
+    g.tile = static_cast<int>(tile);
+    g.stages = stages;
+    g.smem = stage_bytes * stages + 2 * sizeof(uint64_t) * stages;
+    return g;
+}
+
+static int sm_count_current_device(int *out) {
+    static int cached[ZERO_MAX_RANKS] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess && dev < ZERO_MAX_RANKS && cached[dev] > 0) { *out = cached[dev]; return ZERO_OK; }
+    int n = 0;
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
+    if (dev < ZERO_MAX_RANKS) cached[dev] = n;
+    *out = n;
+    return ZERO_OK;
+}
+
+template <int GD, int NR>
+static int launch_pipe_one(int64_t nseg, const KParams &kp, const PipeGeometry &g, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(k_fused_pipe<GD, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(g.smem));
+    if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
+    int sms = 0;
+    const int rc = sm_count_current_device(&sms);
+    if (rc != ZERO_OK) return rc;
+    const int64_t grid = nseg < sms ? nseg : sms;
+    k_fused_pipe<GD, NR><<<static_cast<unsigned>(grid), kPipeThreads, g.smem, st>>>(kp, nseg);
+    return launch_status();
+}
+
+static int launch_pipe(int gd, int nr, int64_t nseg, KParams &kp, cudaStream_t st) {
+    const PipeGeometry g = pipe_geometry(kp.n_ranks, gd);
+    kp.tile = g.tile;
+    kp.stages = g.stages;
+#define ZERO_PIPE_CASE(GDV, NRV) return launch_pipe_one<GDV, NRV>(nseg, kp, g, st)
+    if (gd == ZERO_BF16) {
+        switch (nr) {
+            case 1: ZERO_PIPE_CASE(ZERO_BF16, 1);
+            case 2: ZERO_PIPE_CASE(ZERO_BF16, 2);
+            case 4: ZERO_PIPE_CASE(ZERO_BF16, 4);
+            case 8: ZERO_PIPE_CASE(ZERO_BF16, 8);
+            case 16: ZERO_PIPE_CASE(ZERO_BF16, 16);
+            default: ZERO_PIPE_CASE(ZERO_BF16, 0);
+        }
+    }
+    switch (nr) {
+        case 1: ZERO_PIPE_CASE(ZERO_F32, 1);
+        case 2: ZERO_PIPE_CASE(ZERO_F32, 2);
+        case 4: ZERO_PIPE_CASE(ZERO_F32, 4);
+        case 8: ZERO_PIPE_CASE(ZERO_F32, 8);
+        case 16: ZERO_PIPE_CASE(ZERO_F32, 16);
+        default: ZERO_PIPE_CASE(ZERO_F32, 0);
+    }
+#undef ZERO_PIPE_CASE
+}
 
 }  // namespace zero
 
@@ -567,6 +971,9 @@ extern "C" int zero_plan_attach(zero_plan *plan, void *workspace, size_t bytes, 
     plan->d_partials = reinterpret_cast<double *>(base + L.partials);
     plan->d_sqnorm = reinterpret_cast<double *>(base + L.scalars);
     plan->d_coef = reinterpret_cast<float *>(base + L.scalars + 8);
+    plan->d_err = reinterpret_cast<int *>(base + L.scalars + 16);
+    e = cudaMemsetAsync(base + L.scalars, 0, 256, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
     plan->device = dev;
     plan->attached = true;
     return ZERO_OK;
@@ -714,8 +1121,7 @@ extern "C" int zero_step(const zero_plan *plan, const void *const *grads, int32_
         for (int q = 0; q < n; ++q) kp.grads[q] = grads[q];
         kp.seg_base = begin;
         if (count == 0) return ZERO_OK;
-        launch_k_fused_step(gdtype, n, dim3(static_cast<unsigned>(count)), st, kp);
-        return launch_status();
+        return launch_pipe(gdtype, n, count, kp, st);
     }
     // clipped: norm pass (writes the averaged gradient shard), device
     // coefficient, then the update from the shard scaled by that coefficient
@@ -726,4 +1132,18 @@ extern "C" int zero_step(const zero_plan *plan, const void *const *grads, int32_
     if (count == 0) return ZERO_OK;
     k_adamw_shard<<<static_cast<unsigned>(count), kThreads, 0, st>>>(kp);
     return launch_status();
+}
+
+extern "C" int zero_plan_device_errors(const zero_plan *plan, zero_stream_t stream, int32_t *errors) {
+    int rc = check_attached(plan);
+    if (rc != ZERO_OK) return rc;
+    if (errors == nullptr) return ZERO_EINVAL;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int32_t host = 0;
+    cudaError_t e = cudaMemcpyAsync(&host, plan->d_err, sizeof(host), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(plan->d_err, 0, sizeof(int32_t), st);
+    if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
+    *errors = host;
+    return ZERO_OK;
 }

@@ -249,6 +249,12 @@ int zero_grad_sqnorm_noalloc(const void *const *grads, int32_t n_ranks, int32_t 
 
 /* ---------------------------------------------------------------- diagnostics */
 
+/* Reads and clears the plan's device error word, synchronising `stream`:
+ * *errors = 0 when every bounded wait inside the kernels completed, non-zero
+ * when one gave up (the step it belonged to stopped early and its results are
+ * incomplete).  No kernel waits longer than about two seconds. */
+int zero_plan_device_errors(const zero_plan *plan, zero_stream_t stream, int32_t *errors);
+
 /* Static text for a status code. */
 const char *zero_status_string(int status);
 
