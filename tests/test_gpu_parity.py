@@ -298,6 +298,6 @@ def test_finewrap_full_size_sampled():
 
 @pytest.mark.slow
 def test_4b_zero3_full_size_sampled():
-    c = SampledCase("4b_z3", n_random=200000, extra_units=(32,))
+    c = SampledCase("4b_z3", n_random=300000)
     c.gpu_step(1)
     c.assert_sample_equal(c.oracle_step(1))
