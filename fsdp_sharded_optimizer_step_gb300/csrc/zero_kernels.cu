@@ -40,7 +40,7 @@ struct KParams {
     int32_t write_g, want_partials, use_coef_dev;
     double *partials;       // per segment, indexed by absolute segment number
     int *err;               // device error word (a bounded wait expired)
-    int32_t tile, stages;   // pipeline geometry of k_fused_pipe
+    int32_t tile, stages;   // pipeline geometry of k_pipe
     int64_t p_pad, h_len;   // element counts of full-length and shard buffers (diagnostic bounds checks)
     const float *coef_dev;  // device clip coefficient (NaN: skip the step)
     void *full;
@@ -251,19 +251,67 @@ __device__ __forceinline__ SegSplit split_segment(const Seg &sg) {
     return s;
 }
 
-// ------------------------------------------------------------------ fused step
-// reduce-scatter + average + AdamW + cast + all-gather, one pass.
+// ------------------------------------------------------------------ the three update modes
+// MODE_FUSED:  N gradient rows + master/m/v -> master/m/v + params (one pass)
+// MODE_REDUCE: N gradient rows -> fp32 gradient shard and/or per-segment
+//              binary64 sums of squares of the averaged gradient
+// MODE_SHARD:  fp32 gradient shard (x device clip coefficient) + master/m/v
+//              -> master/m/v + params
+enum { MODE_FUSED = 0, MODE_REDUCE = 1, MODE_SHARD = 2 };
+
+// Per-thread sum of squares without binary64 arithmetic per element (the
+// binary64 rate of this GPU is a small fraction of its binary32 rate): each
+// square is split exactly into a binary32 pair (hi = fl(g*g), lo = fma(g, g,
+// -hi), an error-free product), the pairs are added with TwoSum into a
+// binary32 (hi, lo) accumulator that is renormalised after every add, and
+// the accumulator is widened to binary64 once per segment.  Values whose
+// square would leave the binary32 range (and inf/NaN) go to a binary64
+// accumulator directly.  Relative error per segment and thread is below
+// ~1e-13 for the <= 64 squares a thread adds there.
+struct SqAcc {
+    float hi, lo;
+    double wide;
+};
+
+__device__ __forceinline__ void sq_reset(SqAcc &a) {
+    a.hi = 0.0f;
+    a.lo = 0.0f;
+    a.wide = 0.0;
+}
+
+__device__ __forceinline__ void add_square(SqAcc &a, float g) {
+    const float mag = fabsf(g);
+    if (!(mag <= 0x1p60f) || (mag < 0x1p-60f && mag != 0.0f)) {
+        const double d = static_cast<double>(g);
+        a.wide = __dadd_rn(a.wide, __dmul_rn(d, d));
+        return;
+    }
+    const float ph = __fmul_rn(g, g);
+    const float pl = __fmaf_rn(g, g, -ph);  // exact: g*g - ph
+    const float t = __fadd_rn(a.hi, ph);    // TwoSum(a.hi, ph) = t + e exactly
+    const float bp = __fsub_rn(t, a.hi);
+    const float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(t, bp)), __fsub_rn(ph, bp));
+    const float l = __fadd_rn(a.lo, __fadd_rn(e, pl));
+    a.hi = __fadd_rn(t, l);                 // FastTwoSum renormalisation
+    a.lo = __fsub_rn(l, __fsub_rn(a.hi, t));
+}
+
+__device__ __forceinline__ double sq_total(const SqAcc &a) {
+    return __dadd_rn(__dadd_rn(static_cast<double>(a.hi), static_cast<double>(a.lo)), a.wide);
+}
 
 // Direct (register) path for one segment, spread over nthr threads: the
 // 8-wide groups of [k0, tail0) when `body` is set, and always the head and
-// tail elements.
-template <int GD, int NR>
-__device__ __forceinline__ void fused_direct(const KParams &p, const Seg &sg, const SegSplit &sp, int tid, int nthr,
-                                             bool body) {
+// tail elements.  `coef` scales the gradient when `scale` is set (REDUCE:
+// the host coefficient; SHARD: the device clip coefficient).
+template <int MODE, int GD, int NR>
+__device__ __forceinline__ void direct_segment(const KParams &p, const Seg &sg, const SegSplit &sp, int tid, int nthr,
+                                               bool body, bool scale, float coef, SqAcc &sq) {
     const int r = sg.rank;
     float *__restrict__ W = p.master[r] + sg.s_off;
     float *__restrict__ M = p.m[r] + sg.s_off;
     float *__restrict__ V = p.v[r] + sg.s_off;
+    float *__restrict__ G = p.gshard[r] != nullptr ? p.gshard[r] + sg.s_off : nullptr;
     void *full = p.full;
     void *ps = p.pshard[r];
     if (body) {
@@ -273,57 +321,81 @@ __device__ __forceinline__ void fused_direct(const KParams &p, const Seg &sg, co
                                 aligned_to(W + k, 16),
                             30))
                 continue;
-            float acc[8], w[8], m[8], v[8];
-            fold8<GD, NR>(p, sg.g_off + k, sp.gvec, acc);
-            load8(W + k, w);
-            load8(M + k, m);
-            load8(V + k, v);
-            if (k + 8 > sg.valid) {
+            float g[8];
+            if constexpr (MODE == MODE_SHARD) {
+                load8(G + k, g);
+            } else {
+                float acc[8];
+                fold8<GD, NR>(p, sg.g_off + k, sp.gvec, acc);
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    if (k + e >= sg.valid) acc[e] = 0.0f;
+                for (int e = 0; e < 8; ++e) g[e] = (k + e >= sg.valid) ? 0.0f : average(acc[e], p);
             }
+            if (scale) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) adamw(average(acc[e], p), w[e], m[e], v[e], p.c);
-            store8(W + k, w);
-            store8(M + k, m);
-            store8(V + k, v);
-            if (full != nullptr) store_param8(full, sg.g_off + k, p.pdtype, sp.gvec, w);
-            if (ps != nullptr) store_param8(ps, sg.s_off + k, p.pdtype, true, w);
+                for (int e = 0; e < 8; ++e) g[e] = __fmul_rn(g[e], coef);
+            }
+            if constexpr (MODE == MODE_REDUCE) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) add_square(sq, g[e]);
+                if (G != nullptr && p.write_g) store8(G + k, g);
+            } else {
+                float w[8], m[8], v[8];
+                load8(W + k, w);
+                load8(M + k, m);
+                load8(V + k, v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) adamw(g[e], w[e], m[e], v[e], p.c);
+                store8(W + k, w);
+                store8(M + k, m);
+                store8(V + k, v);
+                if (full != nullptr) store_param8(full, sg.g_off + k, p.pdtype, sp.gvec, w);
+                if (ps != nullptr) store_param8(ps, sg.s_off + k, p.pdtype, true, w);
+            }
         }
     }
-    // head and tail, one element per thread
     const int nedge = sp.k0 + (sg.len - sp.tail0);
     for (int t = tid; t < nedge; t += nthr) {
         const int k = t < sp.k0 ? t : sp.tail0 + (t - sp.k0);
         if (!ZERO_GUARD(k >= 0 && k < sg.len && sg.s_off + k < p.h_len && sg.g_off + k < p.p_pad, 31)) continue;
-        float acc = fold1<GD, NR>(p, sg.g_off + k);
-        if (k >= sg.valid) acc = 0.0f;
-        float w = W[k], m = M[k], v = V[k];
-        adamw(average(acc, p), w, m, v, p.c);
-        W[k] = w;
-        M[k] = m;
-        V[k] = v;
-        if (full != nullptr) store_param1(full, sg.g_off + k, p.pdtype, w);
-        if (ps != nullptr) store_param1(ps, sg.s_off + k, p.pdtype, w);
+        float g;
+        if constexpr (MODE == MODE_SHARD) {
+            g = G[k];
+        } else {
+            g = (k >= sg.valid) ? 0.0f : average(fold1<GD, NR>(p, sg.g_off + k), p);
+        }
+        if (scale) g = __fmul_rn(g, coef);
+        if constexpr (MODE == MODE_REDUCE) {
+            add_square(sq, g);
+            if (G != nullptr && p.write_g) G[k] = g;
+        } else {
+            float w = W[k], m = M[k], v = V[k];
+            adamw(g, w, m, v, p.c);
+            W[k] = w;
+            M[k] = m;
+            V[k] = v;
+            if (full != nullptr) store_param1(full, sg.g_off + k, p.pdtype, w);
+            if (ps != nullptr) store_param1(ps, sg.s_off + k, p.pdtype, w);
+        }
     }
 }
 
-// ------------------------------------------------------------------ fused step, bulk-copy pipeline
+// ------------------------------------------------------------------ bulk-copy pipeline
 // Persistent, warp-specialised: CTA b takes segments b, b + gridDim.x, ...
-// One producer thread streams each aligned segment body, tile by tile, into a
-// ring of `stages` shared-memory buffers with 1-D bulk copies (cp.async.bulk,
-// completion counted in bytes on a per-stage mbarrier): the N gradient rows
-// and master/m/v of `tile` elements.  The consumer warps wait for a stage,
-// compute from shared memory, store master/m/v and the params straight to
-// global memory, and release the stage.  Copies stay in flight while the
-// consumers compute, which the register-only kernel cannot do.  Heads, tails
-// and segments whose gradient positions are not aligned like their shard
-// positions take the direct path in the consumer warps.
+// One producer thread streams each segment body, tile by tile, into a ring of
+// `stages` shared-memory buffers with 1-D bulk copies (cp.async.bulk,
+// completion counted in bytes on a per-stage mbarrier).  The consumer warps
+// wait for a stage, compute from shared memory, store straight to global
+// memory and release the stage; copies stay in flight while they compute.
+// Gradient rows whose positions are not 16-byte aligned are copied as the
+// aligned superset of the tile and read at an element offset (`shift`), so
+// misaligned slices stream like aligned ones.  Heads and tails (before the
+// shard position reaches a multiple of 8, after the last 8-group), and the
+// rare segment whose superset would pass the last whole 16 bytes of a row,
+// take the direct path in the consumer warps.
 //
 // Every wait is bounded (kWaitLimitNs of %globaltimer): on expiry the waiting
-// thread records the failure in *p.err, stops issuing work, and the producer
-// waits (again bounded) for the copies it already issued before the CTA exits.
+// thread records the failure in *p.err and stops waiting; the producer then
+// waits (again bounded) for the copies it already issued before it exits.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *ptr) {
@@ -370,54 +442,194 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     return true;
 }
 
-__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar,
-                                          uint64_t policy) {
-#ifdef ZERO_PIPE_EVICT_FIRST
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
-            smem_u32(dst_smem)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-#else
-    (void)policy;
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      smem_u32(dst_smem)),
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
-#endif
 }
 
-__device__ __forceinline__ uint64_t evict_first_policy() {
-    uint64_t pol = 0;
-#ifdef ZERO_PIPE_EVICT_FIRST
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-#endif
-    return pol;
+// Sync of the consumer warps only (the producer warp does not take part).
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
 }
 
-// Stage layout: N gradient rows of `tile` elements, then master, m, v.
+// Stage layout: gradient rows (room for a shift of up to 7 elements, 16-byte
+// rounded), then master, m, v rows of `tile` fp32.  Shared by host and device.
 struct StageLayout {
-    uint32_t grad_row_bytes, state_off, bytes;
+    uint32_t grad_rows, grad_row_bytes, state_off, bytes;
 };
 
-__device__ __forceinline__ StageLayout stage_layout(int n_ranks, int gbytes, int tile) {
+__host__ __device__ __forceinline__ StageLayout stage_layout(int mode, int n_ranks, int gbytes, int tile) {
     StageLayout L;
-    L.grad_row_bytes = static_cast<uint32_t>(tile * gbytes);
-    L.state_off = L.grad_row_bytes * n_ranks;
-    L.bytes = L.state_off + 3u * static_cast<uint32_t>(tile) * 4u;
+    if (mode == MODE_SHARD) {
+        L.grad_rows = 1;
+        L.grad_row_bytes = static_cast<uint32_t>(tile) * 4u;
+    } else {
+        L.grad_rows = static_cast<uint32_t>(n_ranks);
+        L.grad_row_bytes = (static_cast<uint32_t>(tile + 8) * static_cast<uint32_t>(gbytes) + 15u) & ~15u;
+    }
+    L.state_off = L.grad_rows * L.grad_row_bytes;
+    L.bytes = L.state_off + (mode == MODE_REDUCE ? 0u : 3u * static_cast<uint32_t>(tile) * 4u);
     return L;
 }
 
-template <int GD, int NR>
-__global__ void __launch_bounds__(kPipeThreads, 1) k_fused_pipe(const KParams p, int64_t nseg) {
+// 4 consecutive gradient values from a shared-memory row at element offset
+// `off` (a multiple of 4 plus the row's shift).
+template <int GD, bool ALIGNED>
+__device__ __forceinline__ void smem_load4(const unsigned char *row, int off, float (&x)[4]) {
+    if constexpr (GD == ZERO_BF16) {
+        const unsigned char *b = row + off * 2;
+        uint32_t lo, hi;
+        if (ALIGNED || (off & 3) == 0) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(b);
+            lo = u.x;
+            hi = u.y;
+        } else if ((off & 1) == 0) {
+            lo = *reinterpret_cast<const uint32_t *>(b);
+            hi = *reinterpret_cast<const uint32_t *>(b + 4);
+        } else {
+            const unsigned short *h = reinterpret_cast<const unsigned short *>(b);
+            lo = static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 16);
+            hi = static_cast<uint32_t>(h[2]) | (static_cast<uint32_t>(h[3]) << 16);
+        }
+        x[0] = __uint_as_float(lo << 16);
+        x[1] = __uint_as_float(lo & 0xFFFF0000u);
+        x[2] = __uint_as_float(hi << 16);
+        x[3] = __uint_as_float(hi & 0xFFFF0000u);
+    } else {
+        const float *f = reinterpret_cast<const float *>(row) + off;
+        if (ALIGNED || (off & 3) == 0) {
+            const float4 u = *reinterpret_cast<const float4 *>(f);
+            x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+        } else {
+            x[0] = f[0]; x[1] = f[1]; x[2] = f[2]; x[3] = f[3];
+        }
+    }
+}
+
+// 4 params at element position i of a full-length buffer (ALIGNED: i is a
+// multiple of 4; otherwise any alignment).
+template <bool ALIGNED>
+__device__ __forceinline__ void store_param4(void *base, int64_t i, int32_t pdtype, const float (&w)[4]) {
+    if (pdtype == ZERO_BF16) {
+        unsigned short *d = static_cast<unsigned short *>(base) + i;
+        const uint32_t h0 = f32_to_bf16_rne(w[0]), h1 = f32_to_bf16_rne(w[1]);
+        const uint32_t h2 = f32_to_bf16_rne(w[2]), h3 = f32_to_bf16_rne(w[3]);
+        if (ALIGNED || (i & 3) == 0) {
+            __stcs(reinterpret_cast<uint2 *>(d), make_uint2(h0 | (h1 << 16), h2 | (h3 << 16)));
+        } else if ((i & 1) == 0) {
+            reinterpret_cast<uint32_t *>(d)[0] = h0 | (h1 << 16);
+            reinterpret_cast<uint32_t *>(d)[1] = h2 | (h3 << 16);
+        } else {
+            d[0] = static_cast<unsigned short>(h0);
+            d[1] = static_cast<unsigned short>(h1);
+            d[2] = static_cast<unsigned short>(h2);
+            d[3] = static_cast<unsigned short>(h3);
+        }
+    } else {
+        float *d = static_cast<float *>(base) + i;
+        if (ALIGNED || (i & 3) == 0) {
+            __stcs(reinterpret_cast<float4 *>(d), make_float4(w[0], w[1], w[2], w[3]));
+        } else {
+            d[0] = w[0]; d[1] = w[1]; d[2] = w[2]; d[3] = w[3];
+        }
+    }
+}
+
+// Consumer work on one tile in shared memory: elements [k, k + len) of the
+// segment, 4 per thread per pass.  ALIGNED: the gradient rows have no shift,
+// so every shared-memory read and parameter store is a full vector.
+template <int MODE, int GD, int NR, bool ALIGNED>
+__device__ __forceinline__ void consume_tile(const KParams &p, const Seg &sg, const unsigned char *buf,
+                                             const StageLayout &L, int tile, int k, int len, int shift, int ct,
+                                             bool scale, float coef, SqAcc &sq, float *__restrict__ Wg,
+                                             float *__restrict__ Mg, float *__restrict__ Vg, float *__restrict__ Gg,
+                                             void *full, void *ps, int n) {
+    constexpr int CT = kConsumerWarps * 32;
+    const float *Ws = reinterpret_cast<const float *>(buf + L.state_off);
+    const float *Ms = Ws + tile;
+    const float *Vs = Ms + tile;
+    for (int e = 4 * ct; e < len; e += 4 * CT) {
+        const int kk = k + e;
+        if (!ZERO_GUARD(e + 4 <= tile && sg.s_off + kk + 4 <= p.h_len && sg.g_off + kk + 4 <= p.p_pad &&
+                            aligned_to(Wg + kk, 16) && (!ALIGNED || ((sg.g_off + kk) & 3) == 0),
+                        20))
+            continue;
+        float g[4];
+        if constexpr (MODE == MODE_SHARD) {
+            const float4 u = *reinterpret_cast<const float4 *>(buf + e * 4);
+            g[0] = u.x; g[1] = u.y; g[2] = u.z; g[3] = u.w;
+        } else {
+            float acc[4];
+            smem_load4<GD, ALIGNED>(buf, shift + e, acc);
+#pragma unroll
+            for (int q = 1; q < (NR > 0 ? NR : ZERO_MAX_RANKS); ++q) {
+                if (NR == 0 && q >= n) break;
+                float x[4];
+                smem_load4<GD, ALIGNED>(buf + q * L.grad_row_bytes, shift + e, x);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[i] = __fadd_rn(acc[i], x[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) g[i] = (kk + i >= sg.valid) ? 0.0f : average(acc[i], p);
+        }
+        if (scale) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) g[i] = __fmul_rn(g[i], coef);
+        }
+        if constexpr (MODE == MODE_REDUCE) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) add_square(sq, g[i]);
+            if (Gg != nullptr && p.write_g)
+                __stcs(reinterpret_cast<float4 *>(Gg + kk), make_float4(g[0], g[1], g[2], g[3]));
+        } else {
+            const float4 w4 = *reinterpret_cast<const float4 *>(Ws + e);
+            const float4 m4 = *reinterpret_cast<const float4 *>(Ms + e);
+            const float4 v4 = *reinterpret_cast<const float4 *>(Vs + e);
+            float w[4] = {w4.x, w4.y, w4.z, w4.w}, m[4] = {m4.x, m4.y, m4.z, m4.w}, v[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) adamw(g[i], w[i], m[i], v[i], p.c);
+            __stcs(reinterpret_cast<float4 *>(Wg + kk), make_float4(w[0], w[1], w[2], w[3]));
+            __stcs(reinterpret_cast<float4 *>(Mg + kk), make_float4(m[0], m[1], m[2], m[3]));
+            __stcs(reinterpret_cast<float4 *>(Vg + kk), make_float4(v[0], v[1], v[2], v[3]));
+            if (full != nullptr) store_param4<ALIGNED>(full, sg.g_off + kk, p.pdtype, w);
+            if (ps != nullptr) store_param4<true>(ps, sg.s_off + kk, p.pdtype, w);
+        }
+    }
+}
+
+// Whether the segment body streams through the pipeline (both the producer
+// and the consumers evaluate this identically).
+template <int MODE, int GB>
+__device__ __forceinline__ bool pipe_eligible(const KParams &p, const Seg &sg, const SegSplit &sp) {
+    if (sp.ngroups == 0) return false;
+    if (MODE == MODE_SHARD) return true;
+    const int64_t end_bytes = ((sg.g_off + sp.tail0) * GB + 15) & ~static_cast<int64_t>(15);
+    const int64_t limit = (p.p_pad * GB) & ~static_cast<int64_t>(15);
+    return end_bytes <= limit;
+}
+
+template <int MODE, int GD, int NR>
+__global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64_t nseg) {
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr int GB = GD == ZERO_BF16 ? 2 : 4;
+    constexpr int GB = GD == ZERO_BF16 ? 2 : 4;  // bytes per gradient element
+    constexpr int SHIFT_MASK = 16 / GB - 1;      // elements per 16 bytes, minus one
     const int n = NR > 0 ? NR : p.n_ranks;
     const int tile = p.tile, stages = p.stages;
-    const StageLayout L = stage_layout(n, GB, tile);
+    const StageLayout L = stage_layout(MODE, n, GB, tile);
+    // clip coefficient of a SHARD update (NaN: the global norm was not finite, skip the step)
+    float coef = p.coef;
+    bool scale = MODE == MODE_REDUCE && p.coef != 1.0f;
+    if (MODE == MODE_SHARD && p.use_coef_dev) {
+        coef = *p.coef_dev;
+        if (coef != coef) return;
+        scale = true;
+    }
     uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(stages) * L.bytes);
     uint64_t *empty_bar = full_bar + stages;
     __shared__ int abort_flag;
+    __shared__ double red_smem[kConsumerWarps];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -432,7 +644,6 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_fused_pipe(const KParams p,
     if (warp == kConsumerWarps) {
         // ---------------- producer
         if (lane != 0) return;
-        const uint64_t pol = evict_first_policy();
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;  // per stage: copies issued at least once, parity of the last
@@ -440,8 +651,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_fused_pipe(const KParams p,
         for (int64_t si = blockIdx.x; si < nseg && ok; si += gridDim.x) {
             const Seg sg = p.segs[p.seg_base + si];
             const SegSplit sp = split_segment(sg);
-            if (!sp.gvec) continue;
+            if (!pipe_eligible<MODE, GB>(p, sg, sp)) continue;
             const int r = sg.rank;
+            const int shift = MODE == MODE_SHARD ? 0 : static_cast<int>((sg.g_off + sp.k0) & SHIFT_MASK);
             for (int k = sp.k0; k < sp.tail0; k += tile) {
                 const int len = min(tile, sp.tail0 - k);
                 if (!mbar_wait(&empty_bar[stage], phase ^ 1u) || *reinterpret_cast<volatile int *>(&abort_flag)) {
@@ -449,27 +661,34 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_fused_pipe(const KParams p,
                     break;
                 }
                 unsigned char *buf = smem + static_cast<size_t>(stage) * L.bytes;
-                const uint32_t gbytes = static_cast<uint32_t>(len * GB), sbytes = static_cast<uint32_t>(len * 4);
-                if (!ZERO_GUARD(len > 0 && len <= tile && (gbytes & 15u) == 0 && sg.g_off + k + len <= p.p_pad &&
-                                    sg.s_off + k + len <= p.h_len && r >= 0 && r < n && stage >= 0 && stage < stages,
+                const uint32_t gbytes = MODE == MODE_SHARD
+                                            ? static_cast<uint32_t>(len) * 4u
+                                            : (static_cast<uint32_t>(len + shift) * GB + 15u) & ~15u;
+                const uint32_t sbytes = static_cast<uint32_t>(len) * 4u;
+                if (!ZERO_GUARD(len > 0 && len <= tile && gbytes <= L.grad_row_bytes && sg.g_off + k + len <= p.p_pad &&
+                                    sg.s_off + k + len <= p.h_len && r >= 0 && r < p.n_ranks,
                                 10)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&full_bar[stage], gbytes * n + 3u * sbytes);
-                for (int q = 0; q < n; ++q) {
-                    const unsigned char *src = static_cast<const unsigned char *>(p.grads[q]) + (sg.g_off + k) * GB;
-                    if (ZERO_GUARD(aligned_to(src, 16) && aligned_to(buf + q * L.grad_row_bytes, 16), 11))
-                        bulk_load(buf + q * L.grad_row_bytes, src, gbytes, &full_bar[stage], pol);
+                mbar_arrive_expect_tx(&full_bar[stage], gbytes * L.grad_rows + (MODE == MODE_REDUCE ? 0u : 3u * sbytes));
+                if constexpr (MODE == MODE_SHARD) {
+                    bulk_load(buf, p.gshard[r] + sg.s_off + k, gbytes, &full_bar[stage]);
+                } else {
+                    for (int q = 0; q < n; ++q) {
+                        const unsigned char *src =
+                            static_cast<const unsigned char *>(p.grads[q]) + (sg.g_off + k - shift) * GB;
+                        if (ZERO_GUARD(aligned_to(src, 16), 11))
+                            bulk_load(buf + q * L.grad_row_bytes, src, gbytes, &full_bar[stage]);
+                    }
                 }
-                unsigned char *st = buf + L.state_off;
-                if (ZERO_GUARD(aligned_to(p.master[r] + sg.s_off + k, 16) && aligned_to(p.m[r] + sg.s_off + k, 16) &&
-                                   aligned_to(p.v[r] + sg.s_off + k, 16) && aligned_to(st, 16) &&
-                                   L.state_off + 3u * static_cast<uint32_t>(tile) * 4u <= L.bytes,
-                               12)) {
-                    bulk_load(st, p.master[r] + sg.s_off + k, sbytes, &full_bar[stage], pol);
-                    bulk_load(st + tile * 4, p.m[r] + sg.s_off + k, sbytes, &full_bar[stage], pol);
-                    bulk_load(st + 2 * tile * 4, p.v[r] + sg.s_off + k, sbytes, &full_bar[stage], pol);
+                if constexpr (MODE != MODE_REDUCE) {
+                    unsigned char *st = buf + L.state_off;
+                    if (ZERO_GUARD(aligned_to(p.master[r] + sg.s_off + k, 16), 12)) {
+                        bulk_load(st, p.master[r] + sg.s_off + k, sbytes, &full_bar[stage]);
+                        bulk_load(st + tile * 4, p.m[r] + sg.s_off + k, sbytes, &full_bar[stage]);
+                        bulk_load(st + 2 * tile * 4, p.v[r] + sg.s_off + k, sbytes, &full_bar[stage]);
+                    }
                 }
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -498,101 +717,68 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_fused_pipe(const KParams p,
     constexpr int CT = kConsumerWarps * 32;
     int stage = 0;
     uint32_t phase = 0;
+    bool dead = false;  // a wait gave up: stop consuming, but keep the consumers' barriers matched
     for (int64_t si = blockIdx.x; si < nseg; si += gridDim.x) {
         const Seg sg = p.segs[p.seg_base + si];
         const SegSplit sp = split_segment(sg);
-        fused_direct<GD, NR>(p, sg, sp, ct, CT, !sp.gvec);
-        if (!sp.gvec) continue;
-        const int r = sg.rank;
-        float *__restrict__ Wg = p.master[r] + sg.s_off;
-        float *__restrict__ Mg = p.m[r] + sg.s_off;
-        float *__restrict__ Vg = p.v[r] + sg.s_off;
-        void *full = p.full;
-        void *ps = p.pshard[r];
-        for (int k = sp.k0; k < sp.tail0; k += tile) {
-            const int len = min(tile, sp.tail0 - k);
-            if (!mbar_wait(&full_bar[stage], phase) || *reinterpret_cast<volatile int *>(&abort_flag)) {
-                if (lane == 0) atomicExch(p.err, 2);
-                abort_flag = 1;
-                return;
-            }
-            const unsigned char *buf = smem + static_cast<size_t>(stage) * L.bytes;
-            const float *Ws = reinterpret_cast<const float *>(buf + L.state_off);
-            const float *Ms = Ws + tile;
-            const float *Vs = Ms + tile;
-            for (int e = 4 * ct; e < len; e += 4 * CT) {
-                if (!ZERO_GUARD(e + 4 <= tile && sg.s_off + k + e + 4 <= p.h_len && sg.g_off + k + e + 4 <= p.p_pad &&
-                                    aligned_to(Wg + k + e, 16) && aligned_to(Ws + e, 16) &&
-                                    (full == nullptr || aligned_to(static_cast<unsigned char *>(full) + (sg.g_off + k + e) * (p.pdtype == ZERO_BF16 ? 2 : 4), p.pdtype == ZERO_BF16 ? 8 : 16)),
-                                20))
-                    continue;
-                float acc[4];
-                if constexpr (GD == ZERO_BF16) {
-                    const uint2 x0 = *reinterpret_cast<const uint2 *>(buf + e * 2);
-                    acc[0] = __uint_as_float(x0.x << 16); acc[1] = __uint_as_float(x0.x & 0xFFFF0000u);
-                    acc[2] = __uint_as_float(x0.y << 16); acc[3] = __uint_as_float(x0.y & 0xFFFF0000u);
-#pragma unroll
-                    for (int q = 1; q < (NR > 0 ? NR : ZERO_MAX_RANKS); ++q) {
-                        if (NR == 0 && q >= n) break;
-                        const uint2 x = *reinterpret_cast<const uint2 *>(buf + q * L.grad_row_bytes + e * 2);
-                        acc[0] = __fadd_rn(acc[0], __uint_as_float(x.x << 16));
-                        acc[1] = __fadd_rn(acc[1], __uint_as_float(x.x & 0xFFFF0000u));
-                        acc[2] = __fadd_rn(acc[2], __uint_as_float(x.y << 16));
-                        acc[3] = __fadd_rn(acc[3], __uint_as_float(x.y & 0xFFFF0000u));
-                    }
-                } else {
-                    const float4 x0 = *reinterpret_cast<const float4 *>(buf + e * 4);
-                    acc[0] = x0.x; acc[1] = x0.y; acc[2] = x0.z; acc[3] = x0.w;
-#pragma unroll
-                    for (int q = 1; q < (NR > 0 ? NR : ZERO_MAX_RANKS); ++q) {
-                        if (NR == 0 && q >= n) break;
-                        const float4 x = *reinterpret_cast<const float4 *>(buf + q * L.grad_row_bytes + e * 4);
-                        acc[0] = __fadd_rn(acc[0], x.x);
-                        acc[1] = __fadd_rn(acc[1], x.y);
-                        acc[2] = __fadd_rn(acc[2], x.z);
-                        acc[3] = __fadd_rn(acc[3], x.w);
-                    }
+        const bool piped = pipe_eligible<MODE, GB>(p, sg, sp);
+        SqAcc sq;
+        sq_reset(sq);
+        direct_segment<MODE, GD, NR>(p, sg, sp, ct, CT, !piped, scale, coef, sq);
+        if (piped && !dead) {
+            const int r = sg.rank;
+            const int shift = MODE == MODE_SHARD ? 0 : static_cast<int>((sg.g_off + sp.k0) & SHIFT_MASK);
+            float *__restrict__ Wg = p.master[r] + sg.s_off;
+            float *__restrict__ Mg = p.m[r] + sg.s_off;
+            float *__restrict__ Vg = p.v[r] + sg.s_off;
+            float *__restrict__ Gg = p.gshard[r] != nullptr ? p.gshard[r] + sg.s_off : nullptr;
+            void *full = p.full;
+            void *ps = p.pshard[r];
+            for (int k = sp.k0; k < sp.tail0 && !dead; k += tile) {
+                const int len = min(tile, sp.tail0 - k);
+                if (!mbar_wait(&full_bar[stage], phase) || *reinterpret_cast<volatile int *>(&abort_flag)) {
+                    if (lane == 0) atomicExch(p.err, 2);
+                    abort_flag = 1;
+                    dead = true;
+                    break;
                 }
-                const float4 w4 = *reinterpret_cast<const float4 *>(Ws + e);
-                const float4 m4 = *reinterpret_cast<const float4 *>(Ms + e);
-                const float4 v4 = *reinterpret_cast<const float4 *>(Vs + e);
-                float w[4] = {w4.x, w4.y, w4.z, w4.w}, m[4] = {m4.x, m4.y, m4.z, m4.w}, v[4] = {v4.x, v4.y, v4.z, v4.w};
-                const int kk = k + e;
-                if (kk + 4 > sg.valid) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        if (kk + i >= sg.valid) acc[i] = 0.0f;
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) adamw(average(acc[i], p), w[i], m[i], v[i], p.c);
-                __stcs(reinterpret_cast<float4 *>(Wg + kk), make_float4(w[0], w[1], w[2], w[3]));
-                __stcs(reinterpret_cast<float4 *>(Mg + kk), make_float4(m[0], m[1], m[2], m[3]));
-                __stcs(reinterpret_cast<float4 *>(Vg + kk), make_float4(v[0], v[1], v[2], v[3]));
-                if (p.pdtype == ZERO_BF16) {
-                    const uint2 h = make_uint2(f32_to_bf16_rne(w[0]) | (f32_to_bf16_rne(w[1]) << 16),
-                                               f32_to_bf16_rne(w[2]) | (f32_to_bf16_rne(w[3]) << 16));
-                    if (full != nullptr) __stcs(reinterpret_cast<uint2 *>(static_cast<unsigned short *>(full) + sg.g_off + kk), h);
-                    if (ps != nullptr) __stcs(reinterpret_cast<uint2 *>(static_cast<unsigned short *>(ps) + sg.s_off + kk), h);
-                } else {
-                    const float4 f = make_float4(w[0], w[1], w[2], w[3]);
-                    if (full != nullptr) __stcs(reinterpret_cast<float4 *>(static_cast<float *>(full) + sg.g_off + kk), f);
-                    if (ps != nullptr) __stcs(reinterpret_cast<float4 *>(static_cast<float *>(ps) + sg.s_off + kk), f);
+                const unsigned char *buf = smem + static_cast<size_t>(stage) * L.bytes;
+                // vector path: no gradient-row shift and 4-aligned full positions (the latter is
+                // not implied in SHARD mode, which has no gradient rows)
+                if (shift == 0 && ((sg.g_off + sp.k0) & 3) == 0)
+                    consume_tile<MODE, GD, NR, true>(p, sg, buf, L, tile, k, len, 0, ct, scale, coef, sq, Wg, Mg, Vg, Gg,
+                                                     full, ps, n);
+                else
+                    consume_tile<MODE, GD, NR, false>(p, sg, buf, L, tile, k, len, shift, ct, scale, coef, sq, Wg, Mg,
+                                                      Vg, Gg, full, ps, n);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty_bar[stage]);
+                if (++stage == stages) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_bar[stage]);
-            if (++stage == stages) {
-                stage = 0;
-                phase ^= 1u;
+        }
+        if constexpr (MODE == MODE_REDUCE) {
+            if (p.want_partials) {  // the segment's sum of squares, in a fixed order
+                double x = sq_total(sq);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) x = __dadd_rn(x, __shfl_down_sync(0xFFFFFFFFu, x, o));
+                if (lane == 0) red_smem[warp] = x;
+                consumers_sync();
+                if (warp == 0) {
+                    double t = lane < kConsumerWarps ? red_smem[lane] : 0.0;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) t = __dadd_rn(t, __shfl_down_sync(0xFFFFFFFFu, t, o));
+                    if (lane == 0) p.partials[p.seg_base + si] = t;
+                }
+                consumers_sync();
             }
         }
     }
 }
 
-// ------------------------------------------------------------------ reduce-scatter / sum of squares
-// Writes the averaged (optionally coef-scaled) gradient shard and/or the
-// segment's binary64 sum of squares of the averaged gradient (each square is
-// exact in binary64; the block adds them in a fixed order).
+// ------------------------------------------------------------------ fixed-order total of the sum of squares
 __device__ __forceinline__ double block_sum(double x, double *smem) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x = __dadd_rn(x, __shfl_down_sync(0xFFFFFFFFu, x, o));
@@ -606,43 +792,6 @@ __device__ __forceinline__ double block_sum(double x, double *smem) {
         for (int o = 16; o > 0; o >>= 1) s = __dadd_rn(s, __shfl_down_sync(0xFFFFFFFFu, s, o));
     }
     return s;  // valid in thread 0
-}
-
-template <int GD, int NR>
-__global__ void __launch_bounds__(kThreads, 2) k_reduce(const KParams p) {
-    __shared__ double smem[kThreads / 32];
-    const Seg sg = p.segs[p.seg_base + blockIdx.x];
-    const SegSplit sp = split_segment(sg);
-    float *__restrict__ G = p.write_g ? p.gshard[sg.rank] + sg.s_off : nullptr;
-    const bool scale = p.coef != 1.0f;
-    double sq = 0.0;
-    for (int i = threadIdx.x; i < sp.ngroups; i += kThreads) {
-        const int k = sp.k0 + 8 * i;
-        float acc[8];
-        fold8<GD, NR>(p, sg.g_off + k, sp.gvec, acc);
-        float g[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            g[e] = (k + e >= sg.valid) ? 0.0f : average(acc[e], p);
-            if (scale) g[e] = __fmul_rn(g[e], p.coef);
-            const double d = static_cast<double>(g[e]);
-            sq = __dadd_rn(sq, __dmul_rn(d, d));
-        }
-        if (G != nullptr) store8(G + k, g);
-    }
-    const int nedge = sp.k0 + (sg.len - sp.tail0);
-    for (int t = threadIdx.x; t < nedge; t += kThreads) {
-        const int k = t < sp.k0 ? t : sp.tail0 + (t - sp.k0);
-        float g = (k >= sg.valid) ? 0.0f : average(fold1<GD, NR>(p, sg.g_off + k), p);
-        if (scale) g = __fmul_rn(g, p.coef);
-        const double d = static_cast<double>(g);
-        sq = __dadd_rn(sq, __dmul_rn(d, d));
-        if (G != nullptr) G[k] = g;
-    }
-    if (p.want_partials) {
-        const double s = block_sum(sq, smem);
-        if (threadIdx.x == 0) p.partials[p.seg_base + blockIdx.x] = s;
-    }
 }
 
 // One CTA adds the per-segment partials in a fixed order (thread t takes
@@ -670,55 +819,6 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(const double *partials
             }
             *coef_out = coef;
         }
-    }
-}
-
-// ------------------------------------------------------------------ AdamW from a gradient shard
-__global__ void __launch_bounds__(kThreads, 2) k_adamw_shard(const KParams p) {
-    float coef = 1.0f;
-    if (p.use_coef_dev) {
-        coef = *p.coef_dev;
-        if (coef != coef) return;  // non-finite global norm: the step is skipped
-    }
-    const Seg sg = p.segs[p.seg_base + blockIdx.x];
-    const SegSplit sp = split_segment(sg);
-    const int r = sg.rank;
-    const float *__restrict__ G = p.gshard[r] + sg.s_off;
-    float *__restrict__ W = p.master[r] + sg.s_off;
-    float *__restrict__ M = p.m[r] + sg.s_off;
-    float *__restrict__ V = p.v[r] + sg.s_off;
-    void *full = p.full;
-    void *ps = p.pshard[r];
-    const bool scale = p.use_coef_dev != 0;
-    for (int i = threadIdx.x; i < sp.ngroups; i += kThreads) {
-        const int k = sp.k0 + 8 * i;
-        float g[8], w[8], m[8], v[8];
-        load8(G + k, g);
-        load8(W + k, w);
-        load8(M + k, m);
-        load8(V + k, v);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float ge = scale ? __fmul_rn(g[e], coef) : g[e];
-            adamw(ge, w[e], m[e], v[e], p.c);
-        }
-        store8(W + k, w);
-        store8(M + k, m);
-        store8(V + k, v);
-        if (full != nullptr) store_param8(full, sg.g_off + k, p.pdtype, sp.gvec, w);
-        if (ps != nullptr) store_param8(ps, sg.s_off + k, p.pdtype, true, w);
-    }
-    const int nedge = sp.k0 + (sg.len - sp.tail0);
-    for (int t = threadIdx.x; t < nedge; t += kThreads) {
-        const int k = t < sp.k0 ? t : sp.tail0 + (t - sp.k0);
-        const float ge = scale ? __fmul_rn(G[k], coef) : G[k];
-        float w = W[k], m = M[k], v = V[k];
-        adamw(ge, w, m, v, p.c);
-        W[k] = w;
-        M[k] = m;
-        V[k] = v;
-        if (full != nullptr) store_param1(full, sg.g_off + k, p.pdtype, w);
-        if (ps != nullptr) store_param1(ps, sg.s_off + k, p.pdtype, w);
     }
 }
 
@@ -833,31 +933,6 @@ static int seg_range(const zero_plan *plan, int32_t unit, int64_t &begin, int64_
     return ZERO_OK;
 }
 
-#define ZERO_KERNEL_DISPATCH(kernel)                                                                 \
-    static void launch_##kernel(int gd, int nr, dim3 grid, cudaStream_t st, const KParams &kp) {     \
-        if (gd == ZERO_BF16) {                                                                       \
-            switch (nr) {                                                                            \
-                case 1: kernel<ZERO_BF16, 1><<<grid, kThreads, 0, st>>>(kp); break;                  \
-                case 2: kernel<ZERO_BF16, 2><<<grid, kThreads, 0, st>>>(kp); break;                  \
-                case 4: kernel<ZERO_BF16, 4><<<grid, kThreads, 0, st>>>(kp); break;                  \
-                case 8: kernel<ZERO_BF16, 8><<<grid, kThreads, 0, st>>>(kp); break;                  \
-                case 16: kernel<ZERO_BF16, 16><<<grid, kThreads, 0, st>>>(kp); break;                \
-                default: kernel<ZERO_BF16, 0><<<grid, kThreads, 0, st>>>(kp); break;                 \
-            }                                                                                        \
-        } else {                                                                                     \
-            switch (nr) {                                                                            \
-                case 1: kernel<ZERO_F32, 1><<<grid, kThreads, 0, st>>>(kp); break;                   \
-                case 2: kernel<ZERO_F32, 2><<<grid, kThreads, 0, st>>>(kp); break;                   \
-                case 4: kernel<ZERO_F32, 4><<<grid, kThreads, 0, st>>>(kp); break;                   \
-                case 8: kernel<ZERO_F32, 8><<<grid, kThreads, 0, st>>>(kp); break;                   \
-                case 16: kernel<ZERO_F32, 16><<<grid, kThreads, 0, st>>>(kp); break;                 \
-                default: kernel<ZERO_F32, 0><<<grid, kThreads, 0, st>>>(kp); break;                  \
-            }                                                                                        \
-        }                                                                                            \
-    }
-
-ZERO_KERNEL_DISPATCH(k_reduce)
-
 static bool valid_dtype(int32_t d) { return d == ZERO_BF16 || d == ZERO_F32; }
 
 // ------------------------------------------------------------------ pipeline geometry and launch
@@ -875,22 +950,22 @@ struct PipeGeometry {
 };
 
 // Tile: a multiple of the consumers' pass width (4 elements per consumer
-// thread) close to ZERO_PIPE_STAGE_TARGET bytes per stage (N gradient rows +
-// master/m/v), halved while two stages would not fit the shared-memory
-// budget; then as many stages as fit the budget.
-static PipeGeometry pipe_geometry(int n_ranks, int gdtype) {
+// thread) close to ZERO_PIPE_STAGE_TARGET bytes per stage, halved while two
+// stages would not fit the shared-memory budget; then as many stages as fit.
+static PipeGeometry pipe_geometry(int mode, int n_ranks, int gdtype) {
     const int gb = gdtype == ZERO_BF16 ? 2 : 4;
-    const size_t per_elem = static_cast<size_t>(n_ranks) * gb + 12;
+    const size_t per_elem = mode == MODE_SHARD ? 16 : static_cast<size_t>(n_ranks) * gb + (mode == MODE_FUSED ? 12 : 0);
     const size_t quantum = 4 * kConsumerWarps * 32;
-    size_t mult = ZERO_PIPE_STAGE_TARGET / (quantum * per_elem);
-    size_t tile = quantum * (mult > 0 ? mult : 1);
-    while (tile > 64 && 2 * tile * per_elem > ZERO_PIPE_SMEM_BUDGET) tile >>= 1;
-    const size_t stage_bytes = tile * per_elem;
+    const size_t mult = ZERO_PIPE_STAGE_TARGET / (quantum * per_elem);
+    int tile = static_cast<int>(quantum * (mult > 0 ? mult : 1));
+    while (tile > 64 && 2 * static_cast<size_t>(stage_layout(mode, n_ranks, gb, tile).bytes) > ZERO_PIPE_SMEM_BUDGET)
+        tile >>= 1;
+    const size_t stage_bytes = stage_layout(mode, n_ranks, gb, tile).bytes;
     int stages = static_cast<int>(ZERO_PIPE_SMEM_BUDGET / stage_bytes);
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) stages = 2;
     PipeGeometry g;
-    g.tile = static_cast<int>(tile);
+    g.tile = tile;
     g.stages = stages;
     g.smem = stage_bytes * stages + 2 * sizeof(uint64_t) * stages;
     return g;
@@ -909,43 +984,52 @@ static int sm_count_current_device(int *out) {
     return ZERO_OK;
 }
 
-template <int GD, int NR>
+template <int MODE, int GD, int NR>
 static int launch_pipe_one(int64_t nseg, const KParams &kp, const PipeGeometry &g, cudaStream_t st) {
-    cudaError_t e = cudaFuncSetAttribute(k_fused_pipe<GD, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(k_pipe<MODE, GD, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(g.smem));
     if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
     int sms = 0;
     const int rc = sm_count_current_device(&sms);
     if (rc != ZERO_OK) return rc;
     const int64_t grid = nseg < sms ? nseg : sms;
-    k_fused_pipe<GD, NR><<<static_cast<unsigned>(grid), kPipeThreads, g.smem, st>>>(kp, nseg);
+    k_pipe<MODE, GD, NR><<<static_cast<unsigned>(grid), kPipeThreads, g.smem, st>>>(kp, nseg);
     return launch_status();
 }
 
-static int launch_pipe(int gd, int nr, int64_t nseg, KParams &kp, cudaStream_t st) {
-    const PipeGeometry g = pipe_geometry(kp.n_ranks, gd);
-    kp.tile = g.tile;
-    kp.stages = g.stages;
-#define ZERO_PIPE_CASE(GDV, NRV) return launch_pipe_one<GDV, NRV>(nseg, kp, g, st)
+template <int MODE>
+static int launch_pipe_mode(int gd, int nr, int64_t nseg, const KParams &kp, const PipeGeometry &g, cudaStream_t st) {
     if (gd == ZERO_BF16) {
         switch (nr) {
-            case 1: ZERO_PIPE_CASE(ZERO_BF16, 1);
-            case 2: ZERO_PIPE_CASE(ZERO_BF16, 2);
-            case 4: ZERO_PIPE_CASE(ZERO_BF16, 4);
-            case 8: ZERO_PIPE_CASE(ZERO_BF16, 8);
-            case 16: ZERO_PIPE_CASE(ZERO_BF16, 16);
-            default: ZERO_PIPE_CASE(ZERO_BF16, 0);
+            case 1: return launch_pipe_one<MODE, ZERO_BF16, 1>(nseg, kp, g, st);
+            case 2: return launch_pipe_one<MODE, ZERO_BF16, 2>(nseg, kp, g, st);
+            case 4: return launch_pipe_one<MODE, ZERO_BF16, 4>(nseg, kp, g, st);
+            case 8: return launch_pipe_one<MODE, ZERO_BF16, 8>(nseg, kp, g, st);
+            case 16: return launch_pipe_one<MODE, ZERO_BF16, 16>(nseg, kp, g, st);
+            default: return launch_pipe_one<MODE, ZERO_BF16, 0>(nseg, kp, g, st);
         }
     }
     switch (nr) {
-        case 1: ZERO_PIPE_CASE(ZERO_F32, 1);
-        case 2: ZERO_PIPE_CASE(ZERO_F32, 2);
-        case 4: ZERO_PIPE_CASE(ZERO_F32, 4);
-        case 8: ZERO_PIPE_CASE(ZERO_F32, 8);
-        case 16: ZERO_PIPE_CASE(ZERO_F32, 16);
-        default: ZERO_PIPE_CASE(ZERO_F32, 0);
+        case 1: return launch_pipe_one<MODE, ZERO_F32, 1>(nseg, kp, g, st);
+        case 2: return launch_pipe_one<MODE, ZERO_F32, 2>(nseg, kp, g, st);
+        case 4: return launch_pipe_one<MODE, ZERO_F32, 4>(nseg, kp, g, st);
+        case 8: return launch_pipe_one<MODE, ZERO_F32, 8>(nseg, kp, g, st);
+        case 16: return launch_pipe_one<MODE, ZERO_F32, 16>(nseg, kp, g, st);
+        default: return launch_pipe_one<MODE, ZERO_F32, 0>(nseg, kp, g, st);
     }
-#undef ZERO_PIPE_CASE
+}
+
+// One launch of the pipeline in `mode` over segments [kp.seg_base, kp.seg_base + nseg).
+static int launch_pipe(int mode, int gd, int64_t nseg, KParams &kp, cudaStream_t st) {
+    if (nseg <= 0) return ZERO_OK;
+    const PipeGeometry g = pipe_geometry(mode, kp.n_ranks, gd);
+    kp.tile = g.tile;
+    kp.stages = g.stages;
+    switch (mode) {
+        case MODE_FUSED: return launch_pipe_mode<MODE_FUSED>(gd, kp.n_ranks, nseg, kp, g, st);
+        case MODE_REDUCE: return launch_pipe_mode<MODE_REDUCE>(gd, kp.n_ranks, nseg, kp, g, st);
+        default: return launch_pipe_one<MODE_SHARD, ZERO_F32, 1>(nseg, kp, g, st);  // no gradient rows: one instance
+    }
 }
 
 }  // namespace zero
@@ -995,10 +1079,8 @@ extern "C" int zero_reduce_scatter(const zero_plan *plan, const void *const *gra
         kp.grads[q] = grads[q];
         kp.gshard[q] = gshard[q];
     }
-    const int64_t nseg = static_cast<int64_t>(plan->segs.size());
-    if (nseg == 0) return ZERO_OK;
-    launch_k_reduce(gdtype, n, dim3(static_cast<unsigned>(nseg)), reinterpret_cast<cudaStream_t>(stream), kp);
-    return launch_status();
+    return launch_pipe(MODE_REDUCE, gdtype, static_cast<int64_t>(plan->segs.size()), kp,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 // Pass 1 of a norm: per-segment partial sums (and optionally the gradient
@@ -1014,11 +1096,8 @@ static int launch_norm(const zero_plan *plan, const void *const *grads, int32_t 
         if (gshard != nullptr) kp.gshard[q] = gshard[q];
     }
     const int64_t nseg = static_cast<int64_t>(plan->segs.size());
-    if (nseg > 0) {
-        launch_k_reduce(gdtype, plan->n_ranks, dim3(static_cast<unsigned>(nseg)), st, kp);
-        const int rc = launch_status();
-        if (rc != ZERO_OK) return rc;
-    }
+    const int rc = launch_pipe(MODE_REDUCE, gdtype, nseg, kp, st);
+    if (rc != ZERO_OK) return rc;
     k_finalize<<<1, kFinThreads, 0, st>>>(plan->d_partials, nseg, max_norm, plan->d_sqnorm, sqnorm_out, plan->d_coef);
     return launch_status();
 }
@@ -1065,10 +1144,8 @@ extern "C" int zero_adamw_shard_step(const zero_plan *plan, const float *const *
     fill_common(plan, kp);
     if ((rc = fill_state(plan, kp, master, m, v, pshard, full, pdtype, hp)) != ZERO_OK) return rc;
     for (int q = 0; q < plan->n_ranks; ++q) kp.gshard[q] = const_cast<float *>(gshard[q]);
-    const int64_t nseg = static_cast<int64_t>(plan->segs.size());
-    if (nseg == 0) return ZERO_OK;
-    k_adamw_shard<<<static_cast<unsigned>(nseg), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(kp);
-    return launch_status();
+    return launch_pipe(MODE_SHARD, ZERO_F32, static_cast<int64_t>(plan->segs.size()), kp,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int zero_all_gather(const zero_plan *plan, const void *const *shard, void *full, int32_t pdtype, int32_t unit,
@@ -1120,8 +1197,7 @@ extern "C" int zero_step(const zero_plan *plan, const void *const *grads, int32_
     if (!clip) {
         for (int q = 0; q < n; ++q) kp.grads[q] = grads[q];
         kp.seg_base = begin;
-        if (count == 0) return ZERO_OK;
-        return launch_pipe(gdtype, n, count, kp, st);
+        return launch_pipe(MODE_FUSED, gdtype, count, kp, st);
     }
     // clipped: norm pass (writes the averaged gradient shard), device
     // coefficient, then the update from the shard scaled by that coefficient
@@ -1129,9 +1205,7 @@ extern "C" int zero_step(const zero_plan *plan, const void *const *grads, int32_
     for (int q = 0; q < n; ++q) kp.gshard[q] = gshard_ws[q];
     kp.use_coef_dev = 1;
     kp.coef_dev = plan->d_coef;
-    if (count == 0) return ZERO_OK;
-    k_adamw_shard<<<static_cast<unsigned>(count), kThreads, 0, st>>>(kp);
-    return launch_status();
+    return launch_pipe(MODE_SHARD, ZERO_F32, count, kp, st);
 }
 
 extern "C" int zero_plan_device_errors(const zero_plan *plan, zero_stream_t stream, int32_t *errors) {
