@@ -55,7 +55,7 @@ def measured_hbm_peak():
 def ncu_traffic(workload):
     """Per-launch DRAM bytes (read + write) of the fused kernel from the committed
     ncu summary, or None when the summary is missing or the kernel changed since."""
-    path = os.path.join(ROOT, "profiles", f"k_fused_pipe_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"k_pipe_fused_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -256,21 +256,33 @@ def update_bytes_per_element(cfg):
 E2E_PINNED_BUDGET = 32e9
 
 
-def measure_e2e(args, world, dev, stream, grads, full, step, N, P, gdt, pdt, psi):
-    """Same metric through the public API with host buffers: every step copies the
-    N gradient buffers in from pinned host memory and the gathered params back."""
+def measure_e2e(args, world, dev, stream, grads, full, step, N, P, gdt, pdt, psi, plan=None, state=None, streamed=False):
+    """Same metric through the public API with host buffers: every step takes the
+    N gradient buffers from pinned host memory and returns the gathered params to
+    pinned host memory.  streamed: unit by unit (HostStreamedStep: copy-in of the
+    next unit, update of this one and copy-out of finished ones overlap);
+    otherwise all gradients are copied in, the step runs, the params are copied out."""
     e2e_steps = max(3, min(args.steps, 10))
     h_grads = torch.empty(N, P, dtype=gdt, pin_memory=True)
     for r in range(N):
         h_grads[r].copy_(grads[r])
     h_full = torch.empty(P, dtype=pdt, pin_memory=True)
     torch.cuda.synchronize(dev)
+    if streamed:
+        from fsdp_sharded_optimizer_step_gb300 import workloads as W
+        from fsdp_sharded_optimizer_step_gb300.binding import AdamW
+        from fsdp_sharded_optimizer_step_gb300.streaming import HostStreamedStep
+        streamer = HostStreamedStep(plan, gdt)
+        master, m, v = state
 
-    def e2e_step(t):  # every step: the step's gradients in from pinned host memory, the gathered params out
-        for r in range(N):
-            grads[r].copy_(h_grads[r], non_blocking=True)
-        step(t)
-        h_full.copy_(full, non_blocking=True)
+        def e2e_step(t):
+            streamer.step(h_grads, master, m, v, AdamW(t=t, **W.HP), full, host_full=h_full)
+    else:
+        def e2e_step(t):
+            for r in range(N):
+                grads[r].copy_(h_grads[r], non_blocking=True)
+            step(t)
+            h_full.copy_(full, non_blocking=True)
 
     for t in range(2):  # warm the copy engines
         e2e_step(10_000 + t)
@@ -286,7 +298,9 @@ def measure_e2e(args, world, dev, stream, grads, full, step, N, P, gdt, pdt, psi
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
     e2e = {"value": world * psi / (e2e_ms / 1e3), "unit": UNIT,
            "h2d_bytes_per_step": h_grads.numel() * h_grads.element_size(),
-           "d2h_bytes_per_step": h_full.numel() * h_full.element_size(), "ms_per_step": e2e_ms, "steps": e2e_steps}
+           "d2h_bytes_per_step": h_full.numel() * h_full.element_size(), "ms_per_step": e2e_ms, "steps": e2e_steps,
+           "mode": "streamed per unit: copy-in, update and copy-out overlapped" if streamed
+           else "copy all gradients in, step, copy params out"}
     del h_grads, h_full
     return e2e
 
@@ -386,12 +400,13 @@ def main():
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic, "peak_kind": peak_kind, "bytes_per_element": bpe,
                 "algorithmic_bytes_per_launch": alg_bytes,
-                "kernel": "k_reduce + k_finalize + k_adamw_shard" if clip else "k_fused_pipe"}
+                "kernel": "k_pipe<REDUCE> + k_finalize + k_pipe<SHARD>" if clip else "k_pipe<FUSED>"}
 
     # ---------------- end to end through the public API with host buffers
     pinned_bytes = N * P * grads.element_size() + P * full.element_size()
     if pinned_bytes <= E2E_PINNED_BUDGET:
-        e2e = measure_e2e(args, world, dev, stream, grads, full, step, N, P, gdt, pdt, psi)
+        e2e = measure_e2e(args, world, dev, stream, grads, full, step, N, P, gdt, pdt, psi, plan=plan,
+                          state=(master, m, v), streamed=not (clip or z3 or args.per_unit))
     else:
         e2e = {"value": None, "unit": UNIT, "skipped": f"{pinned_bytes / 1e9:.0f} GB of pinned host buffers "
                                                        f"exceeds the {E2E_PINNED_BUDGET / 1e9:.0f} GB budget"}

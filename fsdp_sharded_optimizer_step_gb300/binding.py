@@ -82,6 +82,8 @@ def lib():
             "zero_all_gather_bf16": (C.c_int, [p, pp, p, i32, p]),
             "zero_step": (C.c_int, [p, pp, i32, pp, pp, pp, p, pp, i32, pp, p, p, i32, p]),
             "zero_grad_sqnorm_noalloc": (C.c_int, [pp, i32, i32, i64, p, p]),
+            "zero_step_unit": (C.c_int, [p, i32, pp, i32, pp, pp, pp, p, pp, i32, p, p]),
+            "zero_reduce_scatter_unit": (C.c_int, [p, i32, pp, i32, pp, f32, p]),
             "zero_plan_device_errors": (C.c_int, [p, p, p]),
             "zero_status_string": (C.c_char_p, [C.c_int]),
             "zero_last_cuda_error": (C.c_int, []),
@@ -332,3 +334,23 @@ def zero_grad_sqnorm_noalloc(grads, sqnorm_out, stream=None):
     arr = (C.c_void_p * len(rows))(*[r.data_ptr() for r in rows])
     _check(lib().zero_grad_sqnorm_noalloc(arr, len(rows), _DTYPES[rows[0].dtype], n, C.c_void_p(sqnorm_out.data_ptr()),
                                           _stream(stream, dev)), "zero_grad_sqnorm_noalloc")
+
+
+def zero_step_unit(plan, unit, grads_unit, master, m, v, hp: AdamW, full=None, pshard=None, stream=None):
+    """The fused step for one unit from unit-local gradient buffers (rank q's S_u positions of the unit)."""
+    g, gd = _rows(plan, grads_unit, plan.S[unit], "grads_unit", _G)
+    W, _ = _rows(plan, master, plan.H, "master", _F)
+    M, _ = _rows(plan, m, plan.H, "m", _F)
+    V, _ = _rows(plan, v, plan.H, "v", _F)
+    fp, ps, pdt = _outputs(plan, full, pshard)
+    c = hp.c()
+    _check(lib().zero_step_unit(plan.handle, int(unit), g, gd, W, M, V, fp, ps, pdt, C.byref(c),
+                                _stream(stream, plan.device)), "zero_step_unit")
+
+
+def zero_reduce_scatter_unit(plan, unit, grads_unit, gshard, coef=1.0, stream=None):
+    """zero_reduce_scatter for one unit from unit-local gradient buffers."""
+    g, gd = _rows(plan, grads_unit, plan.S[unit], "grads_unit", _G)
+    gs, _ = _rows(plan, gshard, plan.H, "gshard", _F)
+    _check(lib().zero_reduce_scatter_unit(plan.handle, int(unit), g, gd, gs, float(coef), _stream(stream, plan.device)),
+           "zero_reduce_scatter_unit")

@@ -41,7 +41,9 @@ struct KParams {
     double *partials;       // per segment, indexed by absolute segment number
     int *err;               // device error word (a bounded wait expired)
     int32_t tile, stages;   // pipeline geometry of k_pipe
-    int64_t p_pad, h_len;   // element counts of full-length and shard buffers (diagnostic bounds checks)
+    int64_t p_pad, h_len;   // element counts of full-length and shard buffers
+    int64_t g_origin;       // full position of element 0 of each gradient row (0, or F_u for unit-local rows)
+    int64_t g_len;          // elements in each gradient row (P_pad, or S_u for unit-local rows)
     const float *coef_dev;  // device clip coefficient (NaN: skip the step)
     void *full;
     const void *grads[ZERO_MAX_RANKS];
@@ -238,16 +240,20 @@ __device__ __forceinline__ void store_param1(void *base, int64_t i, int32_t pdty
 // one element at a time.
 struct SegSplit {
     int k0, ngroups, tail0;
-    bool gvec;  // full/gradient positions are aligned like the shard positions
+    bool gvec;  // gradient positions (relative to the rows' origin) are aligned like the shard positions
+    bool fvec;  // full-buffer positions are aligned like the shard positions
 };
 
-__device__ __forceinline__ SegSplit split_segment(const Seg &sg) {
+// g_origin: the full position held by element 0 of each gradient row (0 for
+// full-length rows, F_u for unit-local rows).
+__device__ __forceinline__ SegSplit split_segment(const Seg &sg, int64_t g_origin) {
     SegSplit s;
     s.k0 = static_cast<int>((8 - (sg.s_off & 7)) & 7);
     if (s.k0 > sg.len) s.k0 = sg.len;
     s.ngroups = (sg.len - s.k0) >> 3;
     s.tail0 = s.k0 + 8 * s.ngroups;
-    s.gvec = ((sg.g_off + s.k0) & 7) == 0;
+    s.gvec = ((sg.g_off - g_origin + s.k0) & 7) == 0;
+    s.fvec = ((sg.g_off + s.k0) & 7) == 0;
     return s;
 }
 
@@ -318,7 +324,7 @@ __device__ __forceinline__ void direct_segment(const KParams &p, const Seg &sg, 
         for (int i = tid; i < sp.ngroups; i += nthr) {
             const int k = sp.k0 + 8 * i;
             if (!ZERO_GUARD(k + 8 <= sg.len && sg.s_off + k + 8 <= p.h_len && sg.g_off + k + 8 <= p.p_pad &&
-                                aligned_to(W + k, 16),
+                                sg.g_off - p.g_origin + k + 8 <= p.g_len && aligned_to(W + k, 16),
                             30))
                 continue;
             float g[8];
@@ -326,7 +332,7 @@ __device__ __forceinline__ void direct_segment(const KParams &p, const Seg &sg, 
                 load8(G + k, g);
             } else {
                 float acc[8];
-                fold8<GD, NR>(p, sg.g_off + k, sp.gvec, acc);
+                fold8<GD, NR>(p, sg.g_off - p.g_origin + k, sp.gvec, acc);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) g[e] = (k + e >= sg.valid) ? 0.0f : average(acc[e], p);
             }
@@ -348,7 +354,7 @@ __device__ __forceinline__ void direct_segment(const KParams &p, const Seg &sg, 
                 store8(W + k, w);
                 store8(M + k, m);
                 store8(V + k, v);
-                if (full != nullptr) store_param8(full, sg.g_off + k, p.pdtype, sp.gvec, w);
+                if (full != nullptr) store_param8(full, sg.g_off + k, p.pdtype, sp.fvec, w);
                 if (ps != nullptr) store_param8(ps, sg.s_off + k, p.pdtype, true, w);
             }
         }
@@ -356,12 +362,15 @@ __device__ __forceinline__ void direct_segment(const KParams &p, const Seg &sg, 
     const int nedge = sp.k0 + (sg.len - sp.tail0);
     for (int t = tid; t < nedge; t += nthr) {
         const int k = t < sp.k0 ? t : sp.tail0 + (t - sp.k0);
-        if (!ZERO_GUARD(k >= 0 && k < sg.len && sg.s_off + k < p.h_len && sg.g_off + k < p.p_pad, 31)) continue;
+        if (!ZERO_GUARD(k >= 0 && k < sg.len && sg.s_off + k < p.h_len && sg.g_off + k < p.p_pad &&
+                            sg.g_off - p.g_origin + k < p.g_len,
+                        31))
+            continue;
         float g;
         if constexpr (MODE == MODE_SHARD) {
             g = G[k];
         } else {
-            g = (k >= sg.valid) ? 0.0f : average(fold1<GD, NR>(p, sg.g_off + k), p);
+            g = (k >= sg.valid) ? 0.0f : average(fold1<GD, NR>(p, sg.g_off - p.g_origin + k), p);
         }
         if (scale) g = __fmul_rn(g, coef);
         if constexpr (MODE == MODE_REDUCE) {
@@ -605,8 +614,8 @@ template <int MODE, int GB>
 __device__ __forceinline__ bool pipe_eligible(const KParams &p, const Seg &sg, const SegSplit &sp) {
     if (sp.ngroups == 0) return false;
     if (MODE == MODE_SHARD) return true;
-    const int64_t end_bytes = ((sg.g_off + sp.tail0) * GB + 15) & ~static_cast<int64_t>(15);
-    const int64_t limit = (p.p_pad * GB) & ~static_cast<int64_t>(15);
+    const int64_t end_bytes = ((sg.g_off - p.g_origin + sp.tail0) * GB + 15) & ~static_cast<int64_t>(15);
+    const int64_t limit = (p.g_len * GB) & ~static_cast<int64_t>(15);
     return end_bytes <= limit;
 }
 
@@ -650,10 +659,10 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64
         bool ok = true;
         for (int64_t si = blockIdx.x; si < nseg && ok; si += gridDim.x) {
             const Seg sg = p.segs[p.seg_base + si];
-            const SegSplit sp = split_segment(sg);
+            const SegSplit sp = split_segment(sg, p.g_origin);
             if (!pipe_eligible<MODE, GB>(p, sg, sp)) continue;
             const int r = sg.rank;
-            const int shift = MODE == MODE_SHARD ? 0 : static_cast<int>((sg.g_off + sp.k0) & SHIFT_MASK);
+            const int shift = MODE == MODE_SHARD ? 0 : static_cast<int>((sg.g_off - p.g_origin + sp.k0) & SHIFT_MASK);
             for (int k = sp.k0; k < sp.tail0; k += tile) {
                 const int len = min(tile, sp.tail0 - k);
                 if (!mbar_wait(&empty_bar[stage], phase ^ 1u) || *reinterpret_cast<volatile int *>(&abort_flag)) {
@@ -666,6 +675,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64
                                             : (static_cast<uint32_t>(len + shift) * GB + 15u) & ~15u;
                 const uint32_t sbytes = static_cast<uint32_t>(len) * 4u;
                 if (!ZERO_GUARD(len > 0 && len <= tile && gbytes <= L.grad_row_bytes && sg.g_off + k + len <= p.p_pad &&
+                                    sg.g_off - p.g_origin + k + len <= p.g_len &&
                                     sg.s_off + k + len <= p.h_len && r >= 0 && r < p.n_ranks,
                                 10)) {
                     ok = false;
@@ -677,7 +687,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64
                 } else {
                     for (int q = 0; q < n; ++q) {
                         const unsigned char *src =
-                            static_cast<const unsigned char *>(p.grads[q]) + (sg.g_off + k - shift) * GB;
+                            static_cast<const unsigned char *>(p.grads[q]) + (sg.g_off - p.g_origin + k - shift) * GB;
                         if (ZERO_GUARD(aligned_to(src, 16), 11))
                             bulk_load(buf + q * L.grad_row_bytes, src, gbytes, &full_bar[stage]);
                     }
@@ -720,14 +730,14 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64
     bool dead = false;  // a wait gave up: stop consuming, but keep the consumers' barriers matched
     for (int64_t si = blockIdx.x; si < nseg; si += gridDim.x) {
         const Seg sg = p.segs[p.seg_base + si];
-        const SegSplit sp = split_segment(sg);
+        const SegSplit sp = split_segment(sg, p.g_origin);
         const bool piped = pipe_eligible<MODE, GB>(p, sg, sp);
         SqAcc sq;
         sq_reset(sq);
         direct_segment<MODE, GD, NR>(p, sg, sp, ct, CT, !piped, scale, coef, sq);
         if (piped && !dead) {
             const int r = sg.rank;
-            const int shift = MODE == MODE_SHARD ? 0 : static_cast<int>((sg.g_off + sp.k0) & SHIFT_MASK);
+            const int shift = MODE == MODE_SHARD ? 0 : static_cast<int>((sg.g_off - p.g_origin + sp.k0) & SHIFT_MASK);
             float *__restrict__ Wg = p.master[r] + sg.s_off;
             float *__restrict__ Mg = p.m[r] + sg.s_off;
             float *__restrict__ Vg = p.v[r] + sg.s_off;
@@ -827,7 +837,7 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(const double *partials
 // vectors where the full position is aligned like the shard position.
 __global__ void __launch_bounds__(kThreads) k_gather(const KParams p) {
     const Seg sg = p.segs[p.seg_base + blockIdx.x];
-    const SegSplit sp = split_segment(sg);
+    const SegSplit sp = split_segment(sg, p.g_origin);
     const int esz = p.pdtype == ZERO_BF16 ? 2 : 4;
     const char *src = static_cast<const char *>(p.pshard[sg.rank]) + sg.s_off * esz;
     char *dst = static_cast<char *>(p.full) + sg.g_off * esz;
@@ -835,7 +845,7 @@ __global__ void __launch_bounds__(kThreads) k_gather(const KParams p) {
         const int k = sp.k0 + 8 * i;
         if (esz == 2) {
             const uint4 x = __ldcs(reinterpret_cast<const uint4 *>(src + k * 2));
-            if (sp.gvec) {
+            if (sp.fvec) {
                 __stcs(reinterpret_cast<uint4 *>(dst + k * 2), x);
             } else {
                 unsigned short *d = reinterpret_cast<unsigned short *>(dst) + k;
@@ -850,7 +860,7 @@ __global__ void __launch_bounds__(kThreads) k_gather(const KParams p) {
             float x[8];
             load8(reinterpret_cast<const float *>(src) + k, x);
             float *d = reinterpret_cast<float *>(dst) + k;
-            if (sp.gvec) {
+            if (sp.fvec) {
                 store8(d, x);
             } else {
 #pragma unroll
@@ -911,6 +921,8 @@ static void fill_common(const zero_plan *plan, KParams &kp) {
     kp.err = plan->d_err;
     kp.p_pad = plan->p_pad;
     kp.h_len = plan->H;
+    kp.g_origin = 0;
+    kp.g_len = plan->p_pad;
 }
 
 static int launch_status() {
@@ -1206,6 +1218,53 @@ extern "C" int zero_step(const zero_plan *plan, const void *const *grads, int32_
     kp.use_coef_dev = 1;
     kp.coef_dev = plan->d_coef;
     return launch_pipe(MODE_SHARD, ZERO_F32, count, kp, st);
+}
+
+// Unit-local variants: grads_unit[q] holds only unit u's S_u padded
+// gradient positions (element i = full position F_u + i).
+static int unit_common(const zero_plan *plan, int32_t unit, const void *const *grads_unit, int32_t gdtype,
+                       int64_t &begin, int64_t &count, KParams &kp) {
+    int rc = check_attached(plan);
+    if (rc != ZERO_OK) return rc;
+    if (!valid_dtype(gdtype) || unit < 0 || unit >= plan->n_units) return ZERO_EINVAL;
+    if ((rc = seg_range(plan, unit, begin, count)) != ZERO_OK) return rc;
+    fill_common(plan, kp);
+    kp.g_origin = plan->F[unit];
+    kp.g_len = plan->S[unit];
+    kp.seg_base = begin;
+    if (plan->S[unit] == 0) return ZERO_OK;
+    if (grads_unit == nullptr) return ZERO_EINVAL;
+    for (int q = 0; q < plan->n_ranks; ++q) {
+        if (grads_unit[q] == nullptr) return ZERO_EINVAL;
+        if (!aligned16(grads_unit[q])) return ZERO_EALIGN;
+        kp.grads[q] = grads_unit[q];
+    }
+    return ZERO_OK;
+}
+
+extern "C" int zero_step_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit, int32_t gdtype,
+                              float *const *master, float *const *m, float *const *v, void *full, void *const *pshard,
+                              int32_t pdtype, const zero_hparams *hp, zero_stream_t stream) {
+    if (hp == nullptr || hp->max_norm > 0.0f) return ZERO_EINVAL;  // a global clip needs every unit
+    int64_t begin = 0, count = 0;
+    KParams kp;
+    int rc = unit_common(plan, unit, grads_unit, gdtype, begin, count, kp);
+    if (rc != ZERO_OK || count == 0) return rc;
+    if ((rc = fill_state(plan, kp, master, m, v, pshard, full, pdtype, hp)) != ZERO_OK) return rc;
+    return launch_pipe(MODE_FUSED, gdtype, count, kp, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int zero_reduce_scatter_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit,
+                                        int32_t gdtype, float *const *gshard, float coef, zero_stream_t stream) {
+    int64_t begin = 0, count = 0;
+    KParams kp;
+    int rc = unit_common(plan, unit, grads_unit, gdtype, begin, count, kp);
+    if (rc != ZERO_OK || count == 0) return rc;
+    if ((rc = check_rank_ptrs(plan, reinterpret_cast<const void *const *>(gshard), true)) != ZERO_OK) return rc;
+    kp.coef = coef;
+    kp.write_g = 1;
+    for (int q = 0; q < plan->n_ranks; ++q) kp.gshard[q] = gshard[q];
+    return launch_pipe(MODE_REDUCE, gdtype, count, kp, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int zero_plan_device_errors(const zero_plan *plan, zero_stream_t stream, int32_t *errors) {

@@ -214,6 +214,27 @@ int zero_step(const zero_plan *plan, const void *const *grads, int32_t gdtype, f
               float *const *gshard_ws, const zero_hparams *hp, double *sqnorm_dev, int32_t unit,
               zero_stream_t stream);
 
+/* ---------------------------------------------------------------- one unit at a time */
+
+/* The fused step for unit `unit` only, with UNIT-LOCAL gradient buffers:
+ * grads_unit[q] (DEVICE, 16-byte aligned) holds rank q's S_u padded gradient
+ * positions of the unit (element i is full position F_u + i), so a caller can
+ * stream gradients in unit by unit (a bucket, or a host-to-device copy) without
+ * ever holding N full gradient buffers ("ZeRO: Three Ledgers, Zero Redundancy",
+ * section 4: gradients streamed through buckets, never resident in full).
+ * master/m/v, full and pshard are the usual full-size buffers (only the unit's
+ * positions are touched).  No clipping (hp->max_norm must be <= 0: a global
+ * norm needs every unit first).  Results equal zero_step's bit for bit.
+ * Errors: as zero_step; ZERO_EINVAL for unit out of [0, n_units) or clipping. */
+int zero_step_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit, int32_t gdtype,
+                   float *const *master, float *const *m, float *const *v, void *full, void *const *pshard,
+                   int32_t pdtype, const zero_hparams *hp, zero_stream_t stream);
+
+/* zero_reduce_scatter for unit `unit` only, from unit-local gradient buffers
+ * (as zero_step_unit): gshard[r][Hoff_u + j] for the unit's slices. */
+int zero_reduce_scatter_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit, int32_t gdtype,
+                             float *const *gshard, float coef, zero_stream_t stream);
+
 /* ---------------------------------------------------------------- without allocation */
 
 /* No counterpart on the pages: an addition for callers that cannot allocate

@@ -131,6 +131,12 @@ def test_argument_errors_are_reported_on_the_host(zlib):
     assert L.zero_reduce_scatter(h, ptrs, B.ZERO_BF16, ptrs, C.c_float(1.0), None) == B.ZERO_ENOTATTACHED
     assert L.zero_all_gather(h, ptrs, C.c_void_p(64), B.ZERO_BF16, -1, None) == B.ZERO_ENOTATTACHED
     assert L.zero_grad_sqnorm(h, ptrs, B.ZERO_BF16, C.c_void_p(64), None) == B.ZERO_ENOTATTACHED
+    assert L.zero_step_unit(h, 0, ptrs, B.ZERO_BF16, ptrs, ptrs, ptrs, None, None, B.ZERO_BF16, C.byref(hp),
+                            None) == B.ZERO_ENOTATTACHED
+    assert L.zero_reduce_scatter_unit(h, 1, ptrs, B.ZERO_BF16, ptrs, C.c_float(1.0), None) == B.ZERO_ENOTATTACHED
+    clip = B.AdamW(max_norm=1.0).c()
+    assert L.zero_step_unit(h, 0, ptrs, B.ZERO_BF16, ptrs, ptrs, ptrs, None, None, B.ZERO_BF16, C.byref(clip),
+                            None) == B.ZERO_EINVAL
     assert L.zero_plan_attach(h, None, 1 << 20, None) == B.ZERO_EINVAL
     assert L.zero_plan_attach(h, C.c_void_p(1 << 12 | 8), 1 << 20, None) == B.ZERO_EALIGN
     assert L.zero_plan_attach(h, C.c_void_p(1 << 12), 8, None) == B.ZERO_ENOMEM

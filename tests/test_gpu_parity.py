@@ -148,6 +148,63 @@ def host_bits_t(x):
     return torch.from_numpy(host_bits(x).astype(np.int64))
 
 
+# ------------------------------------------------------------------ unit-local gradient buffers
+def _unit_rows(c, u):
+    F, S = c.plan.F[u], c.plan.S[u]
+    rows = Z.rank_buffers(c.N, S, c.grads.dtype, c.device)
+    rows.copy_(c.grads[:, F:F + S])
+    return rows
+
+
+@pytest.mark.parametrize("N,gd", [(16, W.BF16), (3, W.F32), (8, W.BF16)])
+def test_unit_local_step_equals_full_step(N, gd):
+    """zero_step_unit over every unit, each from a buffer holding only that unit's
+    gradients (unit offsets F_u of any alignment), equals one zero_step bit for bit."""
+    sizes = W.finewrap_units(n_units=40, lo_log2=0, hi_log2=16, seed=9)
+    a = SmallCase(sizes, N, gd, W.BF16, seed=N)
+    b = SmallCase(sizes, N, gd, W.BF16, seed=N)
+    a.gpu_step(1)
+    hp, _ = hp_for(1)
+    for u in range(len(sizes)):
+        Z.zero_step_unit(b.plan, u, _unit_rows(b, u), b.master, b.m, b.v, hp, full=b.full, pshard=b.pshard)
+    for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v), (a.full, b.full), (a.pshard, b.pshard)):
+        assert torch.equal(host_bits_t(x), host_bits_t(y))
+    assert a.oracle_step(1) == O.OK
+    a.assert_full_equal()
+
+
+def test_unit_local_reduce_scatter_equals_full():
+    sizes = W.finewrap_units(n_units=40, lo_log2=0, hi_log2=16, seed=10)
+    c = SmallCase(sizes, 8, W.BF16, W.BF16, seed=10)
+    Z.zero_reduce_scatter(c.plan, c.grads, c.gshard, coef=0.5)
+    ref = host_bits(c.gshard).copy()
+    c.gshard.zero_()
+    for u in range(len(sizes)):
+        Z.zero_reduce_scatter_unit(c.plan, u, _unit_rows(c, u), c.gshard, coef=0.5)
+    assert np.array_equal(host_bits(c.gshard), ref)
+
+
+def test_host_streamed_step_equals_device_step():
+    """Gradients in pinned host memory, streamed unit by unit with overlapped copies:
+    the same bits as the device-resident step, and the params come back to the host."""
+    from fsdp_sharded_optimizer_step_gb300.streaming import HostStreamedStep
+    sizes = [70001, 3, 65537, 12345, 0, 9, 1 << 20]
+    a = SmallCase(sizes, 8, W.BF16, W.BF16, seed=21)
+    b = SmallCase(sizes, 8, W.BF16, W.BF16, seed=21)
+    host_grads = torch.empty(8, b.plan.P_pad, dtype=torch.bfloat16, pin_memory=True)
+    host_grads.copy_(b.grads.cpu())
+    host_full = torch.zeros(b.plan.P_pad, dtype=torch.bfloat16, pin_memory=True)
+    streamer = HostStreamedStep(b.plan, torch.bfloat16)
+    for t in (1, 2):
+        a.gpu_step(t, pshard=False)
+        hp, _ = hp_for(t)
+        streamer.step(host_grads, b.master, b.m, b.v, hp, b.full, host_full=host_full)
+    torch.cuda.synchronize()
+    for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v), (a.full, b.full)):
+        assert torch.equal(host_bits_t(x), host_bits_t(y))
+    assert np.array_equal(host_bits(host_full), host_bits(a.full))
+
+
 # ------------------------------------------------------------------ unfused parts
 def test_parts_compose_to_the_fused_step():
     """reduce-scatter -> AdamW on the shard -> all-gather == the fused step, bit for bit;
