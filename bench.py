@@ -305,6 +305,148 @@ def measure_e2e(args, world, dev, stream, grads, full, step, N, P, gdt, pdt, psi
     return e2e
 
 
+def run_reshard(args, world, rank, local):
+    """Checkpoint resharding of the workload's master/m/v from N to N' ranks on the
+    device: per step three zero_reshard launches (fp32), 8 bytes of HBM traffic per
+    padded element and array (read + write)."""
+    import fsdp_sharded_optimizer_step_gb300 as Z
+    from fsdp_sharded_optimizer_step_gb300 import build as zbuild
+    from fsdp_sharded_optimizer_step_gb300 import workloads as W
+    zbuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = W.CONFIGS[args.config]
+    sizes = cfg["units"]()
+    N = cfg["N"]
+    N2 = args.to_ranks or 2 * N
+    pf, pt = Z.ZeroPlan(sizes, N, dev), Z.ZeroPlan(sizes, N2, dev)
+    src = W.make_state(N, pf.H, device=dev, out=tuple(Z.rank_buffers(N, pf.H, torch.float32, dev) for _ in range(3)))
+    dst = tuple(Z.rank_buffers(N2, pt.H, torch.float32, dev) for _ in range(3))
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for a, b in zip(src, dst):
+            Z.zero_reshard(pf, pt, a, b)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    nbytes = 3 * (pf.H * N * 4 + pt.H * N2 * 4)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+    if rank == 0:
+        print(json.dumps({"metric": "checkpoint reshard of master/m/v (GB/s of HBM traffic)", "value": world * gbs,
+                          "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                          "dtype": "f32", "data": "synthetic",
+                          "config": {"workload": f"{args.config}: {cfg['desc']}", "from_ranks": N, "to_ranks": N2,
+                                     "bytes_per_step": nbytes},
+                          "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                                       "frac": gbs / peak, "traffic": None, "peak_kind": peak_kind},
+                          "gpu_launches": 3 * args.steps}), flush=True)
+    return 0
+
+
+def _time_ms(fn, stream, reps):
+    fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_unit_flows(args, world, rank, local):
+    """The steps either side of the update, unit by unit (rank 0 of each GPU reports)."""
+    import fsdp_sharded_optimizer_step_gb300 as Z
+    from fsdp_sharded_optimizer_step_gb300 import build as zbuild
+    from fsdp_sharded_optimizer_step_gb300 import workloads as W
+    from fsdp_sharded_optimizer_step_gb300.zero3 import BucketedReduceScatter, UnitGatherer
+    zbuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = W.CONFIGS[args.config]
+    sizes = cfg["units"]()
+    N = cfg["N"]
+    plan = Z.ZeroPlan(sizes, N, dev)
+    P, H = plan.P_pad, plan.H
+    stream = torch.cuda.current_stream(dev)
+    reps = max(args.steps, 1)
+    out = {"n_gpus": world, "steps": reps, "warmup": 1, "data": "synthetic",
+           "config": {"workload": f"{args.config}: {cfg['desc']}", "units": len(sizes)}}
+    if args.op == "zero3_gather":
+        pshard = Z.rank_buffers(N, H, torch.bfloat16, dev)
+        pshard.normal_()
+        gatherers = {"kernel": UnitGatherer(plan, pshard)}
+        d = 1280
+        x = torch.randn(4096, d, dtype=torch.bfloat16, device=dev)
+        wmat = torch.randn(d, 4 * d, dtype=torch.bfloat16, device=dev)
+
+        def compute(u, params_u):  # a synthetic per-unit forward: one GEMM
+            torch.matmul(x, wmat)
+
+        t_compute = _time_ms(lambda: [compute(u, None) for u in range(plan.n_units)], stream, reps)
+        gather_bytes = 2 * P * 2  # bf16 read from the shards + written to the unit buffers
+        timeline = {"compute_only_ms": t_compute, "full_param_buffer_bytes": P * 2,
+                    "unit_buffers_bytes": sum(b.numel() * b.element_size() for b in gatherers["kernel"].buffers)}
+        for e, g in gatherers.items():
+            t_pref = _time_ms(lambda: g.run(compute, prefetch=True), stream, reps)
+            t_serial = _time_ms(lambda: g.run(compute, prefetch=False), stream, reps)
+            t_gather = _time_ms(lambda: g.run(lambda u, p_: None, prefetch=False), stream, reps)
+            timeline[e] = {"prefetch_ms": t_pref, "no_prefetch_ms": t_serial, "gather_only_ms": t_gather,
+                           "gather_GBps": gather_bytes / (t_gather / 1e3) / 1e9,
+                           "hidden_fraction_of_gather": max(0.0, (t_serial - t_pref) / t_gather) if t_gather else None}
+        best = min(timeline[e]["prefetch_ms"] for e in gatherers)
+        out.update(metric="ZeRO-3 forward timeline: per-unit gather + synthetic GEMM (ms per pass)",
+                   value=best, unit="ms", higher_is_better=False, timeline=timeline)
+    else:
+        grads = W.make_grads(N, P, W.BF16, device=dev, out=Z.rank_buffers(N, P, torch.bfloat16, dev))
+        master, m, v = W.make_state(N, H, device=dev,
+                                    out=tuple(Z.rank_buffers(N, H, torch.float32, dev) for _ in range(3)))
+        gshard = Z.rank_buffers(N, H, torch.float32, dev)
+        full = torch.zeros(P, dtype=torch.bfloat16, device=dev)
+        buckets = BucketedReduceScatter(plan)
+        hp = Z.AdamW(t=1, **W.HP)
+
+        def fill(u, view):  # the backward of unit u: here its gradients already exist
+            view.copy_(grads[:, plan.F[u]:plan.F[u] + plan.S[u]])
+
+        def bucketed():
+            for u in reversed(range(plan.n_units)):
+                buckets.reduce(u, fill, gshard)
+            Z.zero_adamw_shard_step(plan, gshard, master, m, v, hp, full=full)
+
+        def rs_units():
+            for u in reversed(range(plan.n_units)):
+                Z.zero_reduce_scatter_unit(plan, u, buckets.bucket[:, :plan.S[u]], gshard)
+
+        t_bucketed = _time_ms(bucketed, stream, reps)
+        t_fill = _time_ms(lambda: [fill(u, buckets.bucket[:, :plan.S[u]]) for u in range(plan.n_units)], stream, reps)
+        t_rs = _time_ms(rs_units, stream, reps)
+        t_shard = _time_ms(lambda: Z.zero_adamw_shard_step(plan, gshard, master, m, v, hp, full=full), stream, reps)
+        t_fused = _time_ms(lambda: Z.zero_step(plan, grads, master, m, v, hp, full=full), stream, reps)
+        out.update(metric="ZeRO-2 bucketed gradient flow: per-unit reduce-scatter + shard update (ms per step)",
+                   value=t_rs + t_shard, unit="ms", higher_is_better=False,
+                   flow={"bucketed_total_ms_incl_fill": t_bucketed, "fill_copies_ms": t_fill,
+                         "reduce_scatter_per_unit_ms": t_rs, "shard_update_ms": t_shard, "fused_step_ms": t_fused,
+                         "bucket_bytes": buckets.bucket_bytes, "full_gradient_bytes": N * P * 2,
+                         "gradient_shard_bytes": N * H * 4})
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -315,12 +457,21 @@ def main():
     ap.add_argument("--per-unit", action="store_true", help="one launch per unit instead of the multi-unit table")
     ap.add_argument("--ref-sample", type=int, default=1 << 22)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--op", default="step", choices=["step", "reshard", "zero3_gather", "zero2_buckets"],
+                    help="step: the sharded optimizer step (default); reshard: checkpoint resharding of the state; "
+                         "zero3_gather: per-unit gathers with/without prefetch beside a synthetic per-unit GEMM; "
+                         "zero2_buckets: bucketed reduce-scatter + shard update against the fused step")
+    ap.add_argument("--to-ranks", type=int, default=0, help="reshard target rank count (default 2N)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.op == "reshard":
+        return run_reshard(args, world, rank, local)
+    if args.op in ("zero3_gather", "zero2_buckets"):
+        return run_unit_flows(args, world, rank, local)
 
     import fsdp_sharded_optimizer_step_gb300 as Z
     from fsdp_sharded_optimizer_step_gb300 import build as zbuild

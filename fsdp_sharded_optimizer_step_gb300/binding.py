@@ -83,6 +83,8 @@ def lib():
             "zero_step": (C.c_int, [p, pp, i32, pp, pp, pp, p, pp, i32, pp, p, p, i32, p]),
             "zero_grad_sqnorm_noalloc": (C.c_int, [pp, i32, i32, i64, p, p]),
             "zero_step_unit": (C.c_int, [p, i32, pp, i32, pp, pp, pp, p, pp, i32, p, p]),
+            "zero_reshard": (C.c_int, [p, p, pp, pp, i32, p]),
+            "zero_all_gather_unit": (C.c_int, [p, i32, pp, p, i32, p]),
             "zero_reduce_scatter_unit": (C.c_int, [p, i32, pp, i32, pp, f32, p]),
             "zero_plan_device_errors": (C.c_int, [p, p, p]),
             "zero_status_string": (C.c_char_p, [C.c_int]),
@@ -354,3 +356,23 @@ def zero_reduce_scatter_unit(plan, unit, grads_unit, gshard, coef=1.0, stream=No
     gs, _ = _rows(plan, gshard, plan.H, "gshard", _F)
     _check(lib().zero_reduce_scatter_unit(plan.handle, int(unit), g, gd, gs, float(coef), _stream(stream, plan.device)),
            "zero_reduce_scatter_unit")
+
+
+def zero_reshard(plan_from, plan_to, src, dst, stream=None):
+    """Remap per-rank shards from plan_from's layout ([N, H]) to plan_to's ([N', H'])."""
+    s, sd = _rows(plan_from, src, plan_from.H, "src", _G)
+    d, dd = _rows(plan_to, dst, plan_to.H, "dst", _G)
+    if sd != dd:
+        raise ValueError("src and dst must have the same dtype")
+    _check(lib().zero_reshard(plan_from.handle, plan_to.handle, s, d, sd, _stream(stream, plan_to.device)),
+           "zero_reshard")
+
+
+def zero_all_gather_unit(plan, unit, shards, dst_unit, stream=None):
+    """Gather one unit's params from the rank shards into a unit-sized buffer (S_u elements)."""
+    s, sd = _rows(plan, shards, plan.H, "shards", _G)
+    dp, dd = _one(plan, dst_unit, plan.S[unit], "dst_unit", _G)
+    if sd != dd:
+        raise ValueError("shards and dst_unit must have the same dtype")
+    _check(lib().zero_all_gather_unit(plan.handle, int(unit), s, dp, sd, _stream(stream, plan.device)),
+           "zero_all_gather_unit")

@@ -27,6 +27,17 @@ static_assert(sizeof(Seg) == 32, "Seg must stay 32 bytes");
 // position that is a multiple of 8, so 32-byte vector access needs no peeling.
 constexpr int32_t kSegMax = 32768;
 
+// Per-unit description, mirrored into the plan's device workspace.
+struct UnitDesc {
+    int64_t F;      // offset of the unit in the full buffer
+    int64_t S;      // padded size (multiple of N)
+    int64_t h;      // slice length S / N
+    int64_t Hoff;   // offset of the unit's slice in every shard buffer
+    int64_t size;   // true size s_u (positions >= size are padding)
+    int64_t seg_begin;  // first launch-table segment of the unit
+};
+static_assert(sizeof(UnitDesc) == 48, "UnitDesc must stay 48 bytes");
+
 // The binary32 constants of one AdamW step, computed once on the host
 // (compiled without FMA contraction) from zero_hparams.
 struct AdamConsts {
@@ -45,6 +56,7 @@ struct zero_plan {
     int64_t p_pad = 0, H = 0;
     std::vector<zero::Seg> segs;           // host copy of the launch table
     std::vector<int64_t> unit_seg_begin;   // [n_units + 1]: segments of unit u
+    std::vector<zero::UnitDesc> unit_table;  // host copy of the device unit table
     // device side, set by zero_plan_attach
     bool attached = false;
     int device = -1;
@@ -53,12 +65,13 @@ struct zero_plan {
     double *d_sqnorm = nullptr;     // S of the last clipped step
     float *d_coef = nullptr;        // clip coefficient of the last clipped step
     int *d_err = nullptr;           // device error word: non-zero after a bounded wait expired
+    zero::UnitDesc *d_units = nullptr;  // device unit table
 };
 
 namespace zero {
 // Workspace layout (byte offsets from the workspace base).
 struct WsLayout {
-    size_t segs, partials, scalars, total;
+    size_t segs, partials, scalars, units, total;
 };
 WsLayout workspace_layout(const zero_plan *plan);
 int adam_consts(const zero_hparams *hp, AdamConsts *out);

@@ -840,12 +840,14 @@ __global__ void __launch_bounds__(kThreads) k_gather(const KParams p) {
     const SegSplit sp = split_segment(sg, p.g_origin);
     const int esz = p.pdtype == ZERO_BF16 ? 2 : 4;
     const char *src = static_cast<const char *>(p.pshard[sg.rank]) + sg.s_off * esz;
-    char *dst = static_cast<char *>(p.full) + sg.g_off * esz;
+    // destination element 0 is full position g_origin (0, or F_u for a unit-sized destination);
+    // sp.gvec is the alignment relative to that origin
+    char *dst = static_cast<char *>(p.full) + (sg.g_off - p.g_origin) * esz;
     for (int i = threadIdx.x; i < sp.ngroups; i += kThreads) {
         const int k = sp.k0 + 8 * i;
         if (esz == 2) {
             const uint4 x = __ldcs(reinterpret_cast<const uint4 *>(src + k * 2));
-            if (sp.fvec) {
+            if (sp.gvec) {
                 __stcs(reinterpret_cast<uint4 *>(dst + k * 2), x);
             } else {
                 unsigned short *d = reinterpret_cast<unsigned short *>(dst) + k;
@@ -860,7 +862,7 @@ __global__ void __launch_bounds__(kThreads) k_gather(const KParams p) {
             float x[8];
             load8(reinterpret_cast<const float *>(src) + k, x);
             float *d = reinterpret_cast<float *>(dst) + k;
-            if (sp.fvec) {
+            if (sp.gvec) {
                 store8(d, x);
             } else {
 #pragma unroll
@@ -1068,6 +1070,12 @@ extern "C" int zero_plan_attach(zero_plan *plan, void *workspace, size_t bytes, 
     plan->d_sqnorm = reinterpret_cast<double *>(base + L.scalars);
     plan->d_coef = reinterpret_cast<float *>(base + L.scalars + 8);
     plan->d_err = reinterpret_cast<int *>(base + L.scalars + 16);
+    if (!plan->unit_table.empty()) {
+        e = cudaMemcpyAsync(base + L.units, plan->unit_table.data(), plan->unit_table.size() * sizeof(UnitDesc),
+                            cudaMemcpyHostToDevice, reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
+    }
+    plan->d_units = reinterpret_cast<UnitDesc *>(base + L.units);
     e = cudaMemsetAsync(base + L.scalars, 0, 256, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
     plan->device = dev;
@@ -1176,6 +1184,28 @@ extern "C" int zero_all_gather(const zero_plan *plan, const void *const *shard, 
     kp.full = full;
     for (int q = 0; q < plan->n_ranks; ++q) kp.pshard[q] = const_cast<void *>(shard[q]);
     if (count == 0) return ZERO_OK;
+    k_gather<<<static_cast<unsigned>(count), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(kp);
+    return launch_status();
+}
+
+extern "C" int zero_all_gather_unit(const zero_plan *plan, int32_t unit, const void *const *shard, void *dst_unit,
+                                    int32_t pdtype, zero_stream_t stream) {
+    int rc = check_attached(plan);
+    if (rc != ZERO_OK) return rc;
+    if (!valid_dtype(pdtype) || unit < 0 || unit >= plan->n_units) return ZERO_EINVAL;
+    int64_t begin = 0, count = 0;
+    if ((rc = seg_range(plan, unit, begin, count)) != ZERO_OK) return rc;
+    if (count == 0) return ZERO_OK;
+    if ((rc = check_rank_ptrs(plan, shard, true)) != ZERO_OK) return rc;
+    if (dst_unit == nullptr) return ZERO_EINVAL;
+    if (!aligned16(dst_unit)) return ZERO_EALIGN;
+    KParams kp;
+    fill_common(plan, kp);
+    kp.seg_base = begin;
+    kp.pdtype = pdtype;
+    kp.full = dst_unit;
+    kp.g_origin = plan->F[unit];
+    for (int q = 0; q < plan->n_ranks; ++q) kp.pshard[q] = const_cast<void *>(shard[q]);
     k_gather<<<static_cast<unsigned>(count), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(kp);
     return launch_status();
 }

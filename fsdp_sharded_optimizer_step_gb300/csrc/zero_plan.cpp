@@ -21,7 +21,8 @@ WsLayout workspace_layout(const zero_plan *plan) {
     L.segs = 0;
     L.partials = round_up(nseg * sizeof(Seg), 256);
     L.scalars = L.partials + round_up(nseg * sizeof(double), 256);
-    L.total = L.scalars + 256;
+    L.units = L.scalars + 256;
+    L.total = L.units + round_up(plan->unit_table.size() * sizeof(UnitDesc), 256);
     return L;
 }
 
@@ -127,6 +128,9 @@ extern "C" int zero_plan_create(const int64_t *unit_sizes, int32_t n_units, int3
             }
         }
         p->unit_seg_begin[n_units] = static_cast<int64_t>(p->segs.size());
+        p->unit_table.resize(n_units);
+        for (int32_t u = 0; u < n_units; ++u)
+            p->unit_table[u] = zero::UnitDesc{p->F[u], p->S[u], p->h[u], p->Hoff[u], p->sizes[u], p->unit_seg_begin[u]};
     } catch (const std::bad_alloc &) {
         delete p;
         return ZERO_ENOMEM;

@@ -1,0 +1,97 @@
+"""ZeRO-3 just-in-time parameter gather with prefetch, and ZeRO-2 bucketed
+gradient reduce-scatter -- the two steps either side of the update.
+
+"ZeRO and FSDP sharding", How it works: per unit, all-gather the bf16 weights,
+compute, free the non-owned part; prefetching unit k+1's all-gather while unit
+k computes keeps it off the critical path, and the peak extra memory is about
+two units of full weights (Complexity and constants).  "ZeRO: Three Ledgers,
+Zero Redundancy", section 4: gradients streamed through buckets never exist in
+full, which is why stage 1 and stage 2 measure the same.
+
+Orchestration only (streams, events, unit-sized buffers); the gathers and
+reduce-scatters run in the CUDA library (zero_all_gather_unit,
+zero_reduce_scatter_unit).
+"""
+import torch
+
+from . import binding as B
+
+
+class UnitGatherer:
+    """Gathers one unit at a time from the rank param shards into one of
+    `n_buffers` unit-sized buffers; with prefetch, unit k+1 is gathered on a side
+    stream while the caller's compute runs on unit k."""
+
+    def __init__(self, plan, pshard, dtype=torch.bfloat16, n_buffers=2):
+        self.plan, self.pshard = plan, pshard
+        dev = plan.device
+        max_s = max(list(plan.S) + [1])
+        per16 = 16 // torch.empty((), dtype=dtype).element_size()
+        stride = (max_s + per16 - 1) // per16 * per16
+        self.buffers = [torch.empty(stride, dtype=dtype, device=dev) for _ in range(n_buffers)]
+        self.side = torch.cuda.Stream(dev)
+        self.ready = [torch.cuda.Event() for _ in range(n_buffers)]
+        self.free = [torch.cuda.Event() for _ in range(n_buffers)]
+
+    def _gather(self, u, b, stream):
+        B.zero_all_gather_unit(self.plan, u, self.pshard, self.buffers[b][:self.plan.S[u]], stream=stream)
+
+    def run(self, compute, order=None, prefetch=True, stream=None):
+        """compute(u, params_u) is called for every unit in `order`, on `stream`
+        (default: the current stream), with params_u the unit's gathered params."""
+        main = stream if stream is not None else torch.cuda.current_stream(self.plan.device)
+        order = list(range(self.plan.n_units)) if order is None else list(order)
+        order = [u for u in order if self.plan.S[u] > 0]
+        nb = len(self.buffers)
+        start = torch.cuda.Event()
+        start.record(main)
+        self.side.wait_event(start)
+        for b in range(nb):
+            self.free[b].record(main)
+
+        def issue(i):
+            b = i % nb
+            if prefetch:
+                self.side.wait_event(self.free[b])
+                self._gather(order[i], b, self.side)
+                self.ready[b].record(self.side)
+            else:
+                self._gather(order[i], b, main)
+
+        if order:
+            issue(0)
+        for i, u in enumerate(order):
+            b = i % nb
+            if prefetch:
+                main.wait_event(self.ready[b])
+                if i + 1 < len(order):
+                    issue(i + 1)
+            compute(u, self.buffers[b][:self.plan.S[u]])
+            self.free[b].record(main)
+            if not prefetch and i + 1 < len(order):
+                issue(i + 1)
+        end = torch.cuda.Event()
+        end.record(self.side)
+        main.wait_event(end)
+
+
+class BucketedReduceScatter:
+    """ZeRO-2 gradient flow through one reusable bucket: fill(u, bucket) writes
+    unit u's N rank gradients (the backward of that unit), and the bucket is
+    reduce-scattered into the fp32 gradient shard right away."""
+
+    def __init__(self, plan, grad_dtype=torch.bfloat16):
+        self.plan = plan
+        self.bucket = B.rank_buffers(plan.n_ranks, max(list(plan.S) + [1]), grad_dtype, plan.device)
+
+    @property
+    def bucket_bytes(self):
+        return self.bucket.shape[0] * self.bucket.stride(0) * self.bucket.element_size()
+
+    def reduce(self, unit, fill, gshard, coef=1.0, stream=None):
+        S = self.plan.S[unit]
+        if S == 0:
+            return
+        view = self.bucket[:, :S]
+        fill(unit, view)
+        B.zero_reduce_scatter_unit(self.plan, unit, view, gshard, coef=coef, stream=stream)

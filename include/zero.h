@@ -216,6 +216,16 @@ int zero_step(const zero_plan *plan, const void *const *grads, int32_t gdtype, f
 
 /* ---------------------------------------------------------------- one unit at a time */
 
+/* All-gather of one unit into a UNIT-SIZED destination: dst_unit (DEVICE,
+ * 16-byte aligned, S_u elements of pdtype) receives the unit's gathered params,
+ * element i = full position F_u + i.  This is ZeRO-3's just-in-time gather
+ * ("ZeRO and FSDP sharding", How it works: per unit, all-gather the bf16
+ * weights, compute, free the non-owned part; prefetching unit k+1's gather
+ * while unit k computes keeps it off the critical path): two unit-sized
+ * buffers instead of the whole parameter buffer. */
+int zero_all_gather_unit(const zero_plan *plan, int32_t unit, const void *const *shard, void *dst_unit,
+                         int32_t pdtype, zero_stream_t stream);
+
 /* The fused step for unit `unit` only, with UNIT-LOCAL gradient buffers:
  * grads_unit[q] (DEVICE, 16-byte aligned) holds rank q's S_u padded gradient
  * positions of the unit (element i is full position F_u + i), so a caller can
@@ -234,6 +244,23 @@ int zero_step_unit(const zero_plan *plan, int32_t unit, const void *const *grads
  * (as zero_step_unit): gshard[r][Hoff_u + j] for the unit's slices. */
 int zero_reduce_scatter_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit, int32_t gdtype,
                              float *const *gshard, float coef, zero_stream_t stream);
+
+/* ---------------------------------------------------------------- checkpoint resharding */
+
+/* Reshard a per-rank array between two layouts of the same units ("ZeRO and
+ * FSDP sharding", Implementation notes: checkpoints are written sharded, each
+ * rank its own shard, and resharded to a different N at load time).
+ *   from, to  attached plans on the current device with identical unit sizes
+ *             (any rank counts, 1..ZERO_MAX_RANKS).
+ *   src       [from N] DEVICE buffers of from's H elements (aligned to the element).
+ *   dst       [to N'] DEVICE buffers of to's H' elements; must not overlap src.
+ *   dtype     ZERO_F32 (master, m, v, gradient shards) or ZERO_BF16 (param shards).
+ * Every real position moves to its owner in the target layout bit for bit;
+ * positions that are padding in the target are written as 0, source padding
+ * is dropped.  One launch; errors as the other calls (ZERO_EINVAL for
+ * mismatched units or devices). */
+int zero_reshard(const zero_plan *from, const zero_plan *to, const void *const *src, void *const *dst,
+                 int32_t dtype, zero_stream_t stream);
 
 /* ---------------------------------------------------------------- without allocation */
 

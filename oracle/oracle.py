@@ -39,6 +39,7 @@ def lib():
             "orc_shard_map": (C.c_int, [p, i32, i32, p]),
             "orc_pad_mask": (C.c_int, [p, i32, i32, p]),
             "orc_locate": (C.c_int, [p, i32, i32, i64, p, p, p, p]),
+            "orc_reshard": (C.c_int, [p, i32, i32, i32, i32, p, p]),
             "orc_avg_grad_array": (C.c_int, [i64, i32, p, i32, p, p]),
             "orc_bf16_rne": (C.c_uint16, [f32]),
             "orc_bf16_rne_array": (None, [i64, p, p]),
@@ -107,6 +108,18 @@ class Plan:
         out = np.zeros(self.P_pad, np.uint8)
         _check(lib().orc_pad_mask(_ptr(self.sizes), len(self.sizes), self.N, _ptr(out)), "pad_mask")
         return out
+
+
+def reshard(sizes, n_from, n_to, src):
+    """src: [n_from, H_from] array (float32 or uint16 bits) -> [n_to, H_to] in the target layout."""
+    sizes = np.ascontiguousarray(sizes, np.int64)
+    src = np.ascontiguousarray(src)
+    H_to = Plan(sizes, n_to).H
+    dst = np.zeros((n_to, H_to), src.dtype)
+    sp = (C.c_void_p * n_from)(*[src[r].ctypes.data for r in range(n_from)])
+    dp = (C.c_void_p * n_to)(*[dst[r].ctypes.data for r in range(n_to)])
+    _check(lib().orc_reshard(_ptr(sizes), len(sizes), n_from, n_to, src.dtype.itemsize, sp, dp), "reshard")
+    return dst
 
 
 # ---------------------------------------------------------------- scalars

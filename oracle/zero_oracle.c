@@ -100,6 +100,38 @@ int orc_shard_map(const int64_t *sizes, int32_t n_units, int32_t n_ranks, int64_
     return ORC_OK;
 }
 
+/* Reshard (checkpoint resharding: "ZeRO and FSDP sharding", Implementation
+ * notes).  dst (n_to rank buffers) receives, for every target rank r and
+ * position j of unit u's slice, the unit position k = r*h'_u + j taken from
+ * the rank that owns k in the source layout; target padding is 0.  Elements
+ * are esize raw bytes. */
+int orc_reshard(const int64_t *sizes, int32_t n_units, int32_t n_from, int32_t n_to, int32_t esize,
+                const void *const *src, void *const *dst)
+{
+    if (n_units < 0 || n_from < 1 || n_to < 1 || (esize != 2 && esize != 4)) return ORC_EINVAL;
+    int64_t hh_from = 0, hh_to = 0;
+    for (int32_t u = 0; u < n_units; ++u) {
+        int64_t s = sizes[u];
+        int64_t S_from = s % n_from == 0 ? s : s + (n_from - s % n_from);
+        int64_t S_to = s % n_to == 0 ? s : s + (n_to - s % n_to);
+        int64_t h_from = S_from / n_from, h_to = S_to / n_to;
+        for (int32_t r = 0; r < n_to; ++r)
+            for (int64_t j = 0; j < h_to; ++j) {
+                int64_t k = (int64_t)r * h_to + j;
+                unsigned char *d = (unsigned char *)dst[r] + (hh_to + j) * esize;
+                if (k < s) {
+                    int64_t rs = k / h_from, js = k % h_from;
+                    memcpy(d, (const unsigned char *)src[rs] + (hh_from + js) * esize, (size_t)esize);
+                } else {
+                    memset(d, 0, (size_t)esize);
+                }
+            }
+        hh_from += h_from;
+        hh_to += h_to;
+    }
+    return ORC_OK;
+}
+
 /* pad[i] = 1 where full position i is padding (position >= s_u inside unit u). */
 int orc_pad_mask(const int64_t *sizes, int32_t n_units, int32_t n_ranks, uint8_t *pad)
 {

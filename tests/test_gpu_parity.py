@@ -358,3 +358,88 @@ def test_4b_zero3_full_size_sampled():
     c = SampledCase("4b_z3", n_random=300000)
     c.gpu_step(1)
     c.assert_sample_equal(c.oracle_step(1))
+
+
+# ------------------------------------------------------------------ checkpoint resharding
+@pytest.mark.parametrize("n_from,n_to", [(8, 16), (16, 8), (8, 3), (3, 8), (5, 5)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_reshard_bit_exact(n_from, n_to, dtype):
+    sizes = W.finewrap_units(n_units=30, lo_log2=0, hi_log2=15, seed=n_from + n_to) + [1, 3, 70001]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pf, pt = Z.ZeroPlan(sizes, n_from, dev), Z.ZeroPlan(sizes, n_to, dev)
+    g = torch.Generator().manual_seed(n_from * 7 + n_to)
+    src_h = torch.randn(n_from, pf.H, generator=g).to(dtype)
+    src = aligned_copy(src_h, dev)
+    dst = Z.rank_buffers(n_to, pt.H, dtype, dev)
+    dst.fill_(7.0)  # every position must be written, padding included
+    Z.zero_reshard(pf, pt, src, dst)
+    want = O.reshard(sizes, n_from, n_to, host_bits(src_h))
+    assert np.array_equal(host_bits(dst), want)
+
+
+def test_sharded_checkpoint_reshard_then_continue(tmp_path):
+    """Save the state of an N=8 run rank by rank, load it into N=4 (resharded on the
+    GPU), continue with N=4 gradients: bit-exact against the oracle, which keeps
+    the state unsharded and only ever changes how it is sliced."""
+    from fsdp_sharded_optimizer_step_gb300 import checkpoint
+    sizes = [70001, 3, 65537, 12345, 9, 1 << 16]
+    c8 = SmallCase(sizes, 8, W.BF16, W.BF16, seed=31)
+    c8.gpu_step(1)
+    assert c8.oracle_step(1) == O.OK
+    checkpoint.save(str(tmp_path), c8.plan, {"master": c8.master, "m": c8.m, "v": c8.v}, step=1)
+    c4 = SmallCase(sizes, 4, W.BF16, W.BF16, seed=32)
+    state, step = checkpoint.load(str(tmp_path), c4.plan)
+    assert step == 1
+    for name, gpu8 in (("master", c8.master), ("m", c8.m), ("v", c8.v)):
+        want = O.reshard(sizes, 8, 4, host_bits(gpu8))
+        assert np.array_equal(host_bits(state[name]), want), name
+        getattr(c4, name).copy_(state[name])
+    # the oracle continues from the same unsharded state (its padding for N=4 holds 0)
+    for arr, src in ((c4.w_o, c4.master), (c4.m_o, c4.m), (c4.v_o, c4.v)):
+        arr[c4.map.ravel()] = src.cpu().numpy().ravel()
+    c4.gpu_step(2)
+    assert c4.oracle_step(2) == O.OK
+    c4.assert_state_equal()
+    c4.assert_full_equal()
+
+
+# ------------------------------------------------------------------ ZeRO-3 gather with prefetch, ZeRO-2 buckets
+def test_zero3_unit_gather_with_prefetch_gives_every_unit_its_params():
+    from fsdp_sharded_optimizer_step_gb300.zero3 import UnitGatherer
+    sizes = [70001, 3, 65537, 12345, 9, 1 << 16, 777]
+    c = SmallCase(sizes, 8, W.BF16, W.BF16, seed=41)
+    c.gpu_step(1)  # fills the param shards (and the full buffer, the reference here)
+    full = host_bits(c.full)
+    seen = {}
+    gatherer = UnitGatherer(c.plan, c.pshard)
+    for prefetch in (True, False):
+        def compute(u, params_u):
+            seen[(prefetch, u)] = params_u.clone()
+        gatherer.run(compute, order=reversed(range(len(sizes))), prefetch=prefetch)
+        torch.cuda.synchronize()
+        for u in range(len(sizes)):
+            F, S = c.plan.F[u], c.plan.S[u]
+            assert np.array_equal(host_bits(seen[(prefetch, u)]), full[F:F + S]), (prefetch, u)
+
+
+def test_zero2_bucketed_reduce_scatter_then_shard_update_equals_fused_step():
+    """Gradients produced unit by unit (reverse order, like a backward pass) into one
+    reused bucket, reduce-scattered at once, then the shard update: the same bits
+    as the fused step that reads N full gradient buffers."""
+    from fsdp_sharded_optimizer_step_gb300.zero3 import BucketedReduceScatter
+    sizes = W.finewrap_units(n_units=25, lo_log2=2, hi_log2=16, seed=12)
+    a = SmallCase(sizes, 8, W.BF16, W.BF16, seed=13)
+    b = SmallCase(sizes, 8, W.BF16, W.BF16, seed=13)
+    a.gpu_step(1, pshard=False)
+    buckets = BucketedReduceScatter(b.plan)
+    assert buckets.bucket_bytes < b.grads.numel() * 2  # never the N full gradient buffers
+
+    def fill(u, view):  # stands in for the backward of unit u
+        view.copy_(b.grads[:, b.plan.F[u]:b.plan.F[u] + b.plan.S[u]])
+
+    for u in reversed(range(len(sizes))):
+        buckets.reduce(u, fill, b.gshard)
+    hp, _ = hp_for(1)
+    Z.zero_adamw_shard_step(b.plan, b.gshard, b.master, b.m, b.v, hp, full=b.full)
+    for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v), (a.full, b.full)):
+        assert torch.equal(host_bits_t(x), host_bits_t(y))

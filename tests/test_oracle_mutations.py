@@ -31,6 +31,7 @@ MUTANTS = [
     ("sqnorm_sum_in_float", "orc_sqacc_add_square(a, orc_avg_grad(n_ranks, grads, gdtype, pad, i));",
      "{ float q = orc_avg_grad(n_ranks, grads, gdtype, pad, i); orc_sqacc_add_square(a, sqrtf(q * q)); }"),
     ("clip_guard_dropped", "double c = (double)max_norm / (sqrt(S) + 1e-6);", "double c = (double)max_norm / sqrt(S);"),
+    ("reshard_wrong_slice", "int64_t rs = k / h_from, js = k % h_from;", "int64_t rs = k / h_to, js = k % h_to;"),
     ("toy_rank_slice", "float acc = c->slots[0][(int64_t)r * h + j];", "float acc = c->slots[0][(int64_t)r * h + j] * 0.5f;"),
 ]
 

@@ -454,3 +454,42 @@ def test_toy_optimizer_floats_per_rank(orc):
     """"ZeRO and FSDP sharding", Code: each rank keeps 3p/n = 750 optimizer floats, not 3p = 3000."""
     p = orc.Plan(W.toy_units(), 4)
     assert 3 * p.H == 750 and 3 * p.P_pad == 3000
+
+
+# ----------------------------------------------------------------------------
+# Checkpoint resharding ("ZeRO and FSDP sharding", Implementation notes: a
+# sharded checkpoint is resharded to a different N at load time).  Pinned to
+# the composition of the two (already pinned) layout maps through the unit
+# positions, and to round trips.
+def _reshard_by_maps(orc, sizes, n_from, n_to, src):
+    pf, pt = orc.Plan(sizes, n_from), orc.Plan(sizes, n_to)
+    full_from = np.zeros(pf.P_pad, src.dtype)
+    full_from[pf.shard_map().ravel()] = src.ravel()
+    full_to = np.zeros(pt.P_pad, src.dtype)
+    for u, s in enumerate(sizes):
+        full_to[pt.F[u]:pt.F[u] + s] = full_from[pf.F[u]:pf.F[u] + s]  # real positions keep their unit position
+    return full_to[pt.shard_map()]
+
+
+@pytest.mark.parametrize("n_from,n_to", [(1, 4), (4, 1), (8, 16), (16, 8), (3, 5), (7, 2), (4, 4)])
+def test_reshard_is_the_composition_of_the_layouts(orc, n_from, n_to):
+    rng = np.random.default_rng(n_from * 31 + n_to)
+    sizes = [int(x) for x in rng.integers(0, 90, 9)] + [1, 257]
+    src = rng.normal(0, 1, (n_from, orc.Plan(sizes, n_from).H)).astype(np.float32)
+    got = orc.reshard(sizes, n_from, n_to, src)
+    assert np.array_equal(got.view(np.uint32), _reshard_by_maps(orc, sizes, n_from, n_to, src).view(np.uint32))
+    bits = rng.integers(0, 1 << 16, src.shape, dtype=np.int64).astype(np.uint16)
+    assert np.array_equal(orc.reshard(sizes, n_from, n_to, bits), _reshard_by_maps(orc, sizes, n_from, n_to, bits))
+
+
+def test_reshard_round_trip_and_identity(orc):
+    rng = np.random.default_rng(3)
+    sizes = [int(x) for x in rng.integers(1, 200, 12)]
+    p8 = orc.Plan(sizes, 8)
+    src = rng.normal(0, 1, (8, p8.H)).astype(np.float32)
+    pad = p8.pad_mask()[p8.shard_map()].astype(bool)
+    src[pad] = 0.0  # padding holds 0, as the update keeps it
+    for n2 in (1, 3, 5, 16):
+        back = orc.reshard(sizes, n2, 8, orc.reshard(sizes, 8, n2, src))
+        assert np.array_equal(back.view(np.uint32), src.view(np.uint32)), n2
+    assert np.array_equal(orc.reshard(sizes, 8, 8, src).view(np.uint32), src.view(np.uint32))
