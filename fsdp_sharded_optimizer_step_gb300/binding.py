@@ -87,6 +87,7 @@ def lib():
             "zero_all_gather_unit": (C.c_int, [p, i32, pp, p, i32, p]),
             "zero_reduce_scatter_unit": (C.c_int, [p, i32, pp, i32, pp, f32, p]),
             "zero_plan_device_errors": (C.c_int, [p, p, p]),
+            "zero_debug_drop_copy": (C.c_int, [i64]),
             "zero_status_string": (C.c_char_p, [C.c_int]),
             "zero_last_cuda_error": (C.c_int, []),
         }
@@ -165,6 +166,11 @@ def zero_plan_device_errors(plan, stream=None):
     _check(lib().zero_plan_device_errors(plan.handle, _stream(stream, plan.device), C.byref(e)),
            "zero_plan_device_errors")
     return e.value
+
+
+def zero_debug_drop_copy(tile):
+    """Testing aid: the next pipelined launch drops one tile's copies in CTA 0 (see include/zero.h)."""
+    _check(lib().zero_debug_drop_copy(int(tile)), "zero_debug_drop_copy")
 
 
 def zero_bias_corrections(t, b1=0.9, b2=0.95):

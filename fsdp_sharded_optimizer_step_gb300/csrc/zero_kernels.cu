@@ -14,6 +14,7 @@
 // and the file is compiled with --fmad=false: nothing is contracted.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -44,6 +45,7 @@ struct KParams {
     int64_t p_pad, h_len;   // element counts of full-length and shard buffers
     int64_t g_origin;       // full position of element 0 of each gradient row (0, or F_u for unit-local rows)
     int64_t g_len;          // elements in each gradient row (P_pad, or S_u for unit-local rows)
+    int64_t drop_tile;      // testing aid: CTA 0 skips the copies of this tile of its sequence (-1: none)
     const float *coef_dev;  // device clip coefficient (NaN: skip the step)
     void *full;
     const void *grads[ZERO_MAX_RANKS];
@@ -657,6 +659,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;  // per stage: copies issued at least once, parity of the last
         bool ok = true;
+        int64_t tile_no = 0;  // position of the tile in this CTA's sequence
         for (int64_t si = blockIdx.x; si < nseg && ok; si += gridDim.x) {
             const Seg sg = p.segs[p.seg_base + si];
             const SegSplit sp = split_segment(sg, p.g_origin);
@@ -680,6 +683,14 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64
                                 10)) {
                     ok = false;
                     break;
+                }
+                if (blockIdx.x == 0 && tile_no++ == p.drop_tile) {
+                    // testing aid: this stage never fills, so its consumers' bounded waits run out
+                    if (++stage == stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    continue;
                 }
                 mbar_arrive_expect_tx(&full_bar[stage], gbytes * L.grad_rows + (MODE == MODE_REDUCE ? 0u : 3u * sbytes));
                 if constexpr (MODE == MODE_SHARD) {
@@ -925,6 +936,7 @@ static void fill_common(const zero_plan *plan, KParams &kp) {
     kp.h_len = plan->H;
     kp.g_origin = 0;
     kp.g_len = plan->p_pad;
+    kp.drop_tile = -1;
 }
 
 static int launch_status() {
@@ -1033,9 +1045,12 @@ static int launch_pipe_mode(int gd, int nr, int64_t nseg, const KParams &kp, con
     }
 }
 
+static std::atomic<int64_t> g_drop_tile{-1};
+
 // One launch of the pipeline in `mode` over segments [kp.seg_base, kp.seg_base + nseg).
 static int launch_pipe(int mode, int gd, int64_t nseg, KParams &kp, cudaStream_t st) {
     if (nseg <= 0) return ZERO_OK;
+    kp.drop_tile = g_drop_tile.exchange(-1);
     const PipeGeometry g = pipe_geometry(mode, kp.n_ranks, gd);
     kp.tile = g.tile;
     kp.stages = g.stages;
@@ -1295,6 +1310,12 @@ extern "C" int zero_reduce_scatter_unit(const zero_plan *plan, int32_t unit, con
     kp.write_g = 1;
     for (int q = 0; q < plan->n_ranks; ++q) kp.gshard[q] = gshard[q];
     return launch_pipe(MODE_REDUCE, gdtype, count, kp, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int zero_debug_drop_copy(int64_t tile) {
+    if (tile < -1) return ZERO_EINVAL;
+    g_drop_tile.store(tile);
+    return ZERO_OK;
 }
 
 extern "C" int zero_plan_device_errors(const zero_plan *plan, zero_stream_t stream, int32_t *errors) {

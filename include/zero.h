@@ -303,6 +303,16 @@ int zero_grad_sqnorm_noalloc(const void *const *grads, int32_t n_ranks, int32_t 
  * incomplete).  No kernel waits longer than about two seconds. */
 int zero_plan_device_errors(const zero_plan *plan, zero_stream_t stream, int32_t *errors);
 
+/* Testing aid for the bounded waits (failure detection without a GPU fault):
+ * arms the NEXT pipelined launch so that its CTA 0 skips the copies of tile
+ * number `tile` of its work (0-based, in issue order).  That stage never fills;
+ * the consumer warps waiting for it give up after about two seconds, the
+ * producer's own wait for the stage runs out next, it waits (bounded) for the
+ * copies it did issue, and the launch ends with incomplete results and a
+ * non-zero device error word (zero_plan_device_errors).  The context stays
+ * usable.  One launch only, then it disarms; -1 disarms at once. */
+int zero_debug_drop_copy(int64_t tile);
+
 /* Static text for a status code. */
 const char *zero_status_string(int status);
 

@@ -443,3 +443,29 @@ def test_zero2_bucketed_reduce_scatter_then_shard_update_equals_fused_step():
     Z.zero_adamw_shard_step(b.plan, b.gshard, b.master, b.m, b.v, hp, full=b.full)
     for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v), (a.full, b.full)):
         assert torch.equal(host_bits_t(x), host_bits_t(y))
+
+
+# ------------------------------------------------------------------ failure detection without a GPU fault
+def test_bounded_wait_runs_out_and_is_reported():
+    """A pipeline stage that never fills (one tile's copies dropped in CTA 0 by the
+    testing aid): the waiting warps give up after about two seconds instead of
+    hanging, the launch ends, the device error word reports it, and the context
+    still runs a correct step afterwards."""
+    import time
+    from fsdp_sharded_optimizer_step_gb300 import binding as B
+    c = SmallCase([70001, 3000], 8, W.BF16, W.BF16, seed=51)
+    assert B.zero_plan_device_errors(c.plan) == 0
+    B.zero_debug_drop_copy(3)
+    t0 = time.time()
+    c.gpu_step(1)
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    assert B.zero_plan_device_errors(c.plan) != 0
+    assert 1.5 < elapsed < 30.0
+    assert B.zero_plan_device_errors(c.plan) == 0  # read-and-clear
+    d = SmallCase([70001, 3000], 8, W.BF16, W.BF16, seed=52)
+    d.gpu_step(1)
+    assert d.oracle_step(1) == O.OK
+    d.assert_state_equal()
+    d.assert_full_equal()
+    assert B.zero_plan_device_errors(d.plan) == 0
