@@ -52,10 +52,11 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def ncu_traffic(workload):
-    """Per-launch DRAM bytes (read + write) of the fused kernel from the committed
-    ncu summary, or None when the summary is missing or the kernel changed since."""
-    path = os.path.join(ROOT, "profiles", f"k_pipe_fused_{workload}.md")
+def ncu_traffic(workload, kind="fused"):
+    """DRAM bytes (read + write) of one step's update launch(es) from the committed
+    ncu summary (kind "fused": the one fused launch; "clip": reduce + finalize +
+    shard), or None when the summary is missing or the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", f"k_pipe_{kind}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -455,6 +456,9 @@ def main():
     ap.add_argument("--config", default="gpt2l")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--per-unit", action="store_true", help="one launch per unit instead of the multi-unit table")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one step's launches in a CUDA graph after the warm-up and replay it in the timed "
+                         "region (removes host launch overhead; the step counter t is the one captured)")
     ap.add_argument("--ref-sample", type=int, default=1 << 22)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--op", default="step", choices=["step", "reshard", "zero3_gather", "zero2_buckets"],
@@ -518,6 +522,15 @@ def main():
     for t in range(1, args.warmup + 1):
         step(t)
     torch.cuda.synchronize(dev)
+    graph = None
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(graph, stream=cap, capture_error_mode="relaxed"):
+            step(args.warmup + 1)
+        stream.wait_stream(cap)
+        torch.cuda.synchronize(dev)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -529,7 +542,12 @@ def main():
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for k in range(args.steps):
-        step(args.warmup + 1 + k, evs[k])
+        if graph is not None:
+            evs[k][0].record(stream)
+            graph.replay()
+            evs[k][1].record(stream)
+        else:
+            step(args.warmup + 1 + k, evs[k])
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -547,7 +565,7 @@ def main():
     alg_bytes = bpe * P
     peak, peak_kind = measured_hbm_peak()
     achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
-    traffic = ncu_traffic(args.config) if not args.per_unit else None
+    traffic = ncu_traffic(args.config, "clip" if clip else "fused") if not args.per_unit else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic, "peak_kind": peak_kind, "bytes_per_element": bpe,
                 "algorithmic_bytes_per_launch": alg_bytes,
@@ -580,7 +598,8 @@ def main():
                 "config": dict(workload_config(args.config, cfg, plan),
                                l2="inputs larger than L2 (no flush): "
                                   f"{alg_bytes / 1e9:.1f} GB of HBM traffic per step vs 129 MB of L2",
-                               launch="one launch per unit" if args.per_unit else "one multi-unit launch",
+                               launch=("one launch per unit" if args.per_unit else "one multi-unit launch")
+                               + (", replayed from one CUDA graph (t fixed at capture)" if args.graph else ""),
                                parallelism=f"{world} GPU(s), each a full replica of the {N}-simulated-rank step"),
                 "hbm_gbs": achieved, "pct_of_peak": 100 * achieved / peak,
                 "pct_of_8tbs_nominal": 100 * achieved / 8000.0,

@@ -272,10 +272,13 @@ enum { MODE_FUSED = 0, MODE_REDUCE = 1, MODE_SHARD = 2 };
 // square is split exactly into a binary32 pair (hi = fl(g*g), lo = fma(g, g,
 // -hi), an error-free product), the pairs are added with TwoSum into a
 // binary32 (hi, lo) accumulator that is renormalised after every add, and
-// the accumulator is widened to binary64 once per segment.  Values whose
-// square would leave the binary32 range (and inf/NaN) go to a binary64
-// accumulator directly.  Relative error per segment and thread is below
-// ~1e-13 for the <= 64 squares a thread adds there.
+// the accumulator is widened to binary64 once per segment.  The pair is
+// error-free only while every bit of g*g is representable: |g| >= 2^-51 keeps
+// the lowest bit of g*g at or above 2^-148 (the error term is never a
+// rounded subnormal), and |g| <= 2^60 keeps 64 squares below 2^128.  Values
+// outside that range (and inf/NaN) go to a binary64 accumulator directly.
+// Relative error per segment and thread is below ~1e-13 for the <= 64
+// squares a thread adds there.
 struct SqAcc {
     float hi, lo;
     double wide;
@@ -289,7 +292,7 @@ __device__ __forceinline__ void sq_reset(SqAcc &a) {
 
 __device__ __forceinline__ void add_square(SqAcc &a, float g) {
     const float mag = fabsf(g);
-    if (!(mag <= 0x1p60f) || (mag < 0x1p-60f && mag != 0.0f)) {
+    if (!(mag <= 0x1p60f) || (mag < 0x1p-51f && mag != 0.0f)) {
         const double d = static_cast<double>(g);
         a.wide = __dadd_rn(a.wide, __dmul_rn(d, d));
         return;

@@ -79,6 +79,10 @@ CONFIGS = {
                             "84,006,400 params), N=8, bf16 grads N(0,1e-3); 3.5 GB of traffic per step",
                        units=lambda: gpt2l_units()[:2], N=8, gdtype=BF16, pdtype=BF16, stage=1, steps=3, max_norm=0.0,
                        grad_sigma=1e-3, master_sigma=0.02),
+    "finewrap_prof": dict(desc="profiling case: 128 fine-wrap units (same law, seed 4), N=16, bf16 grads "
+                               "N(0,1e-3); about 3 GB resident",
+                          units=lambda: finewrap_units(n_units=128), N=16, gdtype=BF16, pdtype=BF16, stage=2, steps=3,
+                          max_norm=0.0, grad_sigma=1e-3, master_sigma=0.02),
     "4b_z3": dict(desc="4B ZeRO-3: N=8, 33 units, bf16 grads N(0,1e-3), per-unit bf16 all-gather",
                   units=llm_4b_units, N=8, gdtype=BF16, pdtype=BF16, stage=3, steps=3, max_norm=0.0,
                   grad_sigma=1e-3, master_sigma=0.02),
@@ -135,3 +139,26 @@ def make_state(n_ranks, length, sigma=0.02, device="cpu", seed=1000, out=None):
     m.zero_()
     v.zero_()
     return master, m, v
+
+
+def wide_range_f32(shape, seed, nonneg=False, subnormal_frac=0.3, wide_frac=0.3, sigma=1e-3):
+    """Seeded fp32 values spanning the whole finite range, as a float32 numpy array.
+
+    A subnormal_frac share has a zero exponent field (subnormals and zeros), a
+    wide_frac share has an exponent field drawn uniformly from 1..254 (up to
+    about 3.4e38), and the rest is N(0, sigma^2).  Signs are random unless
+    nonneg.  Built from bit fields, so every value is finite."""
+    rng = np.random.default_rng(seed)
+    n = int(np.prod(shape))
+    mant = rng.integers(0, 1 << 23, n, dtype=np.uint32)
+    kind = rng.random(n)
+    exp = rng.integers(1, 255, n, dtype=np.uint32)
+    exp[kind < subnormal_frac] = 0
+    bits = (exp << 23) | mant
+    if not nonneg:
+        bits |= rng.integers(0, 2, n, dtype=np.uint32) << 31
+    x = bits.view(np.float32).copy()
+    normal = kind >= subnormal_frac + wide_frac
+    g = rng.normal(0.0, sigma, int(normal.sum()))
+    x[normal] = (np.abs(g) if nonneg else g).astype(np.float32)
+    return x.reshape(shape)

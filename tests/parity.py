@@ -108,6 +108,12 @@ class SmallCase:
         self.out_o = None
         self.S_o = None
 
+    def reload(self):
+        """Re-read the oracle's copies after a test overwrote the GPU inputs."""
+        for name, src in (("w_o", self.master), ("m_o", self.m), ("v_o", self.v)):
+            getattr(self, name)[self.map.ravel()] = src.cpu().numpy().ravel()
+        self.g_o = oracle_grad_rows(self.grads)
+
     # -------------------------------------------------------------- runs
     def gpu_step(self, t, max_norm=0.0, full=True, pshard=True, unit=-1, **over):
         hp, _ = hp_for(t, max_norm, **over)

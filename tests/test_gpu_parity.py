@@ -144,6 +144,32 @@ def test_per_unit_launches_equal_one_multi_unit_launch():
         assert torch.equal(host_bits_t(x), host_bits_t(y))
 
 
+def test_per_unit_steps_replay_from_a_cuda_graph():
+    """The per-unit launches of one step captured in a CUDA graph (the library
+    makes no synchronising or allocating call on that path) and replayed: the
+    result equals the oracle's step bit for bit; a second replay repeats the
+    captured step (the step counter is a launch argument)."""
+    sizes = [5000, 3, 70000, 1, 40961]
+    c = SmallCase(sizes, 8, W.BF16, W.BF16, seed=33)
+    c.gpu_step(1, unit=0)  # first launch of each kernel outside the capture
+    c.reload()
+    hp, _ = hp_for(2)
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=side, capture_error_mode="relaxed"):
+        for u in range(len(sizes)):
+            Z.zero_step(c.plan, c.grads, c.master, c.m, c.v, hp, full=c.full, pshard=c.pshard, unit=u)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        assert c.oracle_step(2) == O.OK
+        c.assert_state_equal()
+        c.assert_full_equal()
+        c.assert_pshard_equal()
+
+
 def host_bits_t(x):
     return torch.from_numpy(host_bits(x).astype(np.int64))
 

@@ -6,6 +6,7 @@ mistake in the oracle would do to it.
 import json
 import math
 import os
+from concurrent.futures import ThreadPoolExecutor
 from fractions import Fraction
 
 import numpy as np
@@ -256,6 +257,34 @@ def test_bf16_matches_library_conversion(orc):
     o = ours[nan]
     assert np.all((o & 0x7F80) == 0x7F80) and np.all((o & 0x7F) | 0x40 != 0) and np.all(o & 0x40)
     assert np.array_equal(o & 0x8000, (b[nan] >> 16).astype(np.uint16) & 0x8000)
+
+
+def test_bf16_exhaustive_against_library_conversion(orc):
+    """Every one of the 2^32 binary32 bit patterns: the oracle's cast equals
+    torch's float->bfloat16 conversion on all non-NaN inputs; NaN inputs (two
+    known ranges of bit patterns) give a quiet NaN of the same sign."""
+    ch = 1 << 24
+    base = np.arange(ch, dtype=np.uint32)
+    nan_ranges = [(0x7F800001, 0x80000000), (0xFF800001, 1 << 32)]
+
+    def check(c):
+        lo = c * ch
+        b = base + np.uint32(lo)
+        x = b.view(np.float32)
+        ours = orc.bf16_rne_array(x)
+        ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        ne = ours != ref
+        for a, e in nan_ranges:
+            s, t = max(a, lo) - lo, min(e, lo + ch) - lo
+            if s < t:
+                ne[s:t] = False
+                o = ours[s:t]
+                assert np.all((o & 0x7F80) == 0x7F80) and np.all(o & 0x40)
+                assert np.array_equal(o >> 15, (b[s:t] >> 31).astype(np.uint16))
+        return int(np.count_nonzero(ne))
+
+    with ThreadPoolExecutor(os.cpu_count() or 1) as ex:  # the oracle's C call releases the GIL
+        assert sum(ex.map(check, range((1 << 32) // ch))) == 0
 
 
 def test_bf16_matches_exact_rounding(orc):
