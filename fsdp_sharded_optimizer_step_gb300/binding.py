@@ -169,7 +169,7 @@ def zero_plan_device_errors(plan, stream=None):
 
 
 def zero_debug_drop_copy(tile):
-    """Testing aid: the next pipelined launch drops one tile's copies in CTA 0 (see include/zero.h)."""
+    """Testing aid: the next pipelined launch drops the copies of one tile of its first segment (see include/zero.h)."""
     _check(lib().zero_debug_drop_copy(int(tile)), "zero_debug_drop_copy")
 
 

@@ -65,6 +65,7 @@ struct zero_plan {
     double *d_sqnorm = nullptr;     // S of the last clipped step
     float *d_coef = nullptr;        // clip coefficient of the last clipped step
     int *d_err = nullptr;           // device error word: non-zero after a bounded wait expired
+    unsigned long long *d_tickets = nullptr;  // [2]: segment tickets and finished CTAs of a pipelined launch
     zero::UnitDesc *d_units = nullptr;  // device unit table
 };
 

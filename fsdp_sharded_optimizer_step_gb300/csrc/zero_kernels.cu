@@ -28,6 +28,7 @@ constexpr int kThreads = 256;
 #endif
 constexpr int kConsumerWarps = ZERO_PIPE_CONSUMER_WARPS;
 constexpr int kPipeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kSegRing = 8;  // segment numbers the producer may take ahead of its consumers
 
 struct KParams {
     const Seg *segs;
@@ -45,7 +46,8 @@ struct KParams {
     int64_t p_pad, h_len;   // element counts of full-length and shard buffers
     int64_t g_origin;       // full position of element 0 of each gradient row (0, or F_u for unit-local rows)
     int64_t g_len;          // elements in each gradient row (P_pad, or S_u for unit-local rows)
-    int64_t drop_tile;      // testing aid: CTA 0 skips the copies of this tile of its sequence (-1: none)
+    int64_t drop_tile;      // testing aid: the copies of this tile of segment 0 are skipped (-1: none)
+    unsigned long long *tickets;  // k_pipe's schedule: [0] next segment ticket, [1] CTAs done (0, 0 between launches)
     const float *coef_dev;  // device clip coefficient (NaN: skip the step)
     void *full;
     const void *grads[ZERO_MAX_RANKS];
@@ -394,8 +396,14 @@ __device__ __forceinline__ void direct_segment(const KParams &p, const Seg &sg, 
 }
 
 // ------------------------------------------------------------------ bulk-copy pipeline
-// Persistent, warp-specialised: CTA b takes segments b, b + gridDim.x, ...
-// One producer thread streams each segment body, tile by tile, into a ring of
+// Persistent, warp-specialised, dynamically scheduled: each CTA's producer
+// thread takes the next segment of the launch table from the plan's ticket
+// counter when it is ready for more work, and hands the segment number to its
+// consumer warps through a small shared-memory ring.  Segments are handed out
+// in table order, so the CTAs always work on neighbouring parts of the
+// buffers, and every CTA finishes within about one segment of the others
+// however unequal the segments are.
+// The producer streams each segment body, tile by tile, into a ring of
 // `stages` shared-memory buffers with 1-D bulk copies (cp.async.bulk,
 // completion counted in bytes on a per-stage mbarrier).  The consumer warps
 // wait for a stage, compute from shared memory, store straight to global
@@ -461,11 +469,6 @@ __device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint3
                      smem_u32(dst_smem)),
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
-}
-
-// Sync of the consumer warps only (the producer warp does not take part).
-__device__ __forceinline__ void consumers_sync() {
-    asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
 }
 
 // Stage layout: gradient rows (room for a shift of up to 7 elements, 16-byte
@@ -643,12 +646,23 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64
     uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(stages) * L.bytes);
     uint64_t *empty_bar = full_bar + stages;
     __shared__ int abort_flag;
-    __shared__ double red_smem[kConsumerWarps];
+    // segment ring: the producer publishes each segment number it took (-1: no more) in
+    // seg_ring[slot] and arrives on seg_full[slot]; every consumer warp arrives on
+    // seg_empty[slot] once done with the number (warp 0 only after the segment's sum of
+    // squares, which it adds up from red_smem[slot] once red_full[slot] completes)
+    __shared__ int64_t seg_ring[kSegRing];
+    __shared__ __align__(8) uint64_t seg_full[kSegRing], seg_empty[kSegRing], red_full[kSegRing];
+    __shared__ double red_smem[kSegRing][kConsumerWarps];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], kConsumerWarps);
+        }
+        for (int s = 0; s < kSegRing; ++s) {
+            mbar_init(&seg_full[s], 1);
+            mbar_init(&seg_empty[s], kConsumerWarps);
+            mbar_init(&red_full[s], kConsumerWarps);
         }
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -662,8 +676,27 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;  // per stage: copies issued at least once, parity of the last
         bool ok = true;
-        int64_t tile_no = 0;  // position of the tile in this CTA's sequence
-        for (int64_t si = blockIdx.x; si < nseg && ok; si += gridDim.x) {
+        int rs = 0;
+        uint32_t rphase = 0;
+        // the next ticket is taken as soon as a segment is published, so the atomic's latency
+        // overlaps the copies of the segment at hand
+        unsigned long long next_ticket = atomicAdd(&p.tickets[0], 1ull);
+        for (;;) {
+            const unsigned long long t = next_ticket;
+            const int64_t si = ok && t < static_cast<unsigned long long>(nseg) ? static_cast<int64_t>(t) : -1;
+            if (!mbar_wait(&seg_empty[rs], rphase ^ 1u)) {  // the consumers stopped taking segments
+                ok = false;
+                break;
+            }
+            *reinterpret_cast<volatile int64_t *>(&seg_ring[rs]) = si;
+            mbar_arrive(&seg_full[rs]);  // release: the number is visible to the warps that see the phase
+            if (++rs == kSegRing) {
+                rs = 0;
+                rphase ^= 1u;
+            }
+            if (si < 0) break;
+            next_ticket = atomicAdd(&p.tickets[0], 1ull);
+            int64_t tile_no = 0;  // position of the tile in its segment
             const Seg sg = p.segs[p.seg_base + si];
             const SegSplit sp = split_segment(sg, p.g_origin);
             if (!pipe_eligible<MODE, GB>(p, sg, sp)) continue;
@@ -687,7 +720,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64
                     ok = false;
                     break;
                 }
-                if (blockIdx.x == 0 && tile_no++ == p.drop_tile) {
+                if (si == 0 && tile_no++ == p.drop_tile) {
                     // testing aid: this stage never fills, so its consumers' bounded waits run out
                     if (++stage == stages) {
                         stage = 0;
@@ -729,6 +762,12 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64
             for (int s = 0; s < stages; ++s)
                 if (issued_mask & (1u << s)) mbar_wait(&full_bar[s], (issued_parity >> s) & 1u);
         }
+        // every producer has taken its last ticket before it counts itself done, so the last
+        // one can re-arm the counter for the next launch (which a CUDA graph may replay as is)
+        if (atomicAdd(&p.tickets[1], 1ull) == static_cast<unsigned long long>(gridDim.x) - 1ull) {
+            atomicExch(&p.tickets[0], 0ull);
+            atomicExch(&p.tickets[1], 0ull);
+        }
         return;
     }
 
@@ -741,8 +780,27 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64
     constexpr int CT = kConsumerWarps * 32;
     int stage = 0;
     uint32_t phase = 0;
-    bool dead = false;  // a wait gave up: stop consuming, but keep the consumers' barriers matched
-    for (int64_t si = blockIdx.x; si < nseg; si += gridDim.x) {
+    bool dead = false;  // a stage wait gave up: stop consuming tiles, keep taking part in the rings
+    int rs = 0;
+    uint32_t rphase = 0;
+    for (;;) {
+        // wait results are made warp-uniform: the lanes of a warp must take the same path
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&seg_full[rs], rphase))) {  // no segment number in time: give up
+            if (lane == 0) atomicExch(p.err, 3);
+            abort_flag = 1;
+            break;
+        }
+        const int64_t si = *reinterpret_cast<volatile int64_t *>(&seg_ring[rs]);
+        const int slot = rs;
+        const uint32_t slot_phase = rphase;
+        if (++rs == kSegRing) {
+            rs = 0;
+            rphase ^= 1u;
+        }
+        const bool reduce_here = MODE == MODE_REDUCE && p.want_partials && si >= 0;
+        __syncwarp();
+        if (lane == 0 && !(reduce_here && warp == 0)) mbar_arrive(&seg_empty[slot]);
+        if (si < 0) break;
         const Seg sg = p.segs[p.seg_base + si];
         const SegSplit sp = split_segment(sg, p.g_origin);
         const bool piped = pipe_eligible<MODE, GB>(p, sg, sp);
@@ -760,7 +818,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64
             void *ps = p.pshard[r];
             for (int k = sp.k0; k < sp.tail0 && !dead; k += tile) {
                 const int len = min(tile, sp.tail0 - k);
-                if (!mbar_wait(&full_bar[stage], phase) || *reinterpret_cast<volatile int *>(&abort_flag)) {
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full_bar[stage], phase) &&
+                                                 !*reinterpret_cast<volatile int *>(&abort_flag))) {
                     if (lane == 0) atomicExch(p.err, 2);
                     abort_flag = 1;
                     dead = true;
@@ -788,15 +847,27 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64
                 double x = sq_total(sq);
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) x = __dadd_rn(x, __shfl_down_sync(0xFFFFFFFFu, x, o));
-                if (lane == 0) red_smem[warp] = x;
-                consumers_sync();
-                if (warp == 0) {
-                    double t = lane < kConsumerWarps ? red_smem[lane] : 0.0;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) t = __dadd_rn(t, __shfl_down_sync(0xFFFFFFFFu, t, o));
-                    if (lane == 0) p.partials[p.seg_base + si] = t;
+                if (lane == 0) {
+                    red_smem[slot][warp] = x;
+                    mbar_arrive(&red_full[slot]);  // release: warp 0 sees x once the phase completes
                 }
-                consumers_sync();
+                if (warp == 0) {
+                    // warp 0 hands the slot back (seg_empty) only after this read, so no warp can
+                    // write a later segment's value into red_smem[slot] before it
+                    if (__all_sync(0xFFFFFFFFu, mbar_wait(&red_full[slot], slot_phase))) {
+                        double t = lane < kConsumerWarps
+                                       ? *reinterpret_cast<volatile double *>(&red_smem[slot][lane])
+                                       : 0.0;
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) t = __dadd_rn(t, __shfl_down_sync(0xFFFFFFFFu, t, o));
+                        if (lane == 0) p.partials[p.seg_base + si] = t;
+                    } else {
+                        if (lane == 0) atomicExch(p.err, 4);
+                        abort_flag = 1;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&seg_empty[slot]);
+                }
             }
         }
     }
@@ -940,6 +1011,7 @@ static void fill_common(const zero_plan *plan, KParams &kp) {
     kp.g_origin = 0;
     kp.g_len = plan->p_pad;
     kp.drop_tile = -1;
+    kp.tickets = plan->d_tickets;
 }
 
 static int launch_status() {
@@ -1088,6 +1160,7 @@ extern "C" int zero_plan_attach(zero_plan *plan, void *workspace, size_t bytes, 
     plan->d_sqnorm = reinterpret_cast<double *>(base + L.scalars);
     plan->d_coef = reinterpret_cast<float *>(base + L.scalars + 8);
     plan->d_err = reinterpret_cast<int *>(base + L.scalars + 16);
+    plan->d_tickets = reinterpret_cast<unsigned long long *>(base + L.scalars + 24);
     if (!plan->unit_table.empty()) {
         e = cudaMemcpyAsync(base + L.units, plan->unit_table.data(), plan->unit_table.size() * sizeof(UnitDesc),
                             cudaMemcpyHostToDevice, reinterpret_cast<cudaStream_t>(stream));

@@ -56,7 +56,13 @@
  *     live in a caller-provided workspace (zero_plan_attach).
  *   - Device work is asynchronous on the given stream (NULL = legacy default
  *     stream).  Calls that use the same plan's workspace must be ordered on one
- *     stream, or otherwise serialised by the caller.
+ *     stream, or otherwise serialised by the caller.  Every call that updates,
+ *     reduces or scatters (everything but the gathers, the norm without a
+ *     plan and the reshard) hands its work out to the GPU's SMs from a counter
+ *     in the workspace; two such calls on one plan running at the same time
+ *     would take work from each other and leave parts undone.  The counter is
+ *     back at zero when each call's kernel ends, so captured calls replay
+ *     correctly from a CUDA graph.
  *   - Arrays of rank pointers ("[N]") are HOST arrays of N DEVICE pointers.
  *     Every device pointer must be 16-byte aligned (ZERO_EALIGN otherwise).
  *   - A plan is immutable after zero_plan_attach and may be shared by threads
@@ -304,8 +310,8 @@ int zero_grad_sqnorm_noalloc(const void *const *grads, int32_t n_ranks, int32_t 
 int zero_plan_device_errors(const zero_plan *plan, zero_stream_t stream, int32_t *errors);
 
 /* Testing aid for the bounded waits (failure detection without a GPU fault):
- * arms the NEXT pipelined launch so that its CTA 0 skips the copies of tile
- * number `tile` of its work (0-based, in issue order).  That stage never fills;
+ * arms the NEXT pipelined launch so that the copies of tile number `tile`
+ * (0-based) of the launch's first segment are skipped.  That stage never fills;
  * the consumer warps waiting for it give up after about two seconds, the
  * producer's own wait for the stage runs out next, it waits (bounded) for the
  * copies it did issue, and the launch ends with incomplete results and a

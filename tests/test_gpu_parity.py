@@ -473,7 +473,7 @@ def test_zero2_bucketed_reduce_scatter_then_shard_update_equals_fused_step():
 
 # ------------------------------------------------------------------ failure detection without a GPU fault
 def test_bounded_wait_runs_out_and_is_reported():
-    """A pipeline stage that never fills (one tile's copies dropped in CTA 0 by the
+    """A pipeline stage that never fills (one tile's copies dropped in the first segment by the
     testing aid): the waiting warps give up after about two seconds instead of
     hanging, the launch ends, the device error word reports it, and the context
     still runs a correct step afterwards."""
