@@ -16,6 +16,7 @@ import torch
 from . import build as _build
 
 ZERO_OK, ZERO_EINVAL, ZERO_ENOMEM, ZERO_ECUDA, ZERO_EALIGN, ZERO_ENOTATTACHED, ZERO_ERANGE = 0, -1, -2, -3, -4, -7, -8
+ZERO_ENONFINITE, ZERO_ETIMEOUT = -5, -6
 ZERO_F32, ZERO_BF16 = 0, 1
 ZERO_MAX_RANKS = 64
 
@@ -87,6 +88,7 @@ def lib():
             "zero_all_gather_unit": (C.c_int, [p, i32, pp, p, i32, p]),
             "zero_reduce_scatter_unit": (C.c_int, [p, i32, pp, i32, pp, f32, p]),
             "zero_plan_device_errors": (C.c_int, [p, p, p]),
+            "zero_plan_check": (C.c_int, [p, p]),
             "zero_debug_drop_copy": (C.c_int, [i64]),
             "zero_status_string": (C.c_char_p, [C.c_int]),
             "zero_last_cuda_error": (C.c_int, []),
@@ -166,6 +168,16 @@ def zero_plan_device_errors(plan, stream=None):
     _check(lib().zero_plan_device_errors(plan.handle, _stream(stream, plan.device), C.byref(e)),
            "zero_plan_device_errors")
     return e.value
+
+
+def zero_plan_check(plan, stream=None):
+    """Status of the device work queued on the plan since the last check (synchronises the stream):
+    ZERO_OK, ZERO_ETIMEOUT (a bounded wait expired) or ZERO_ENONFINITE (a clipped step was skipped
+    because its global norm was not finite).  Clears both conditions; argument errors raise."""
+    rc = lib().zero_plan_check(plan.handle, _stream(stream, plan.device))
+    if rc in (ZERO_OK, ZERO_ETIMEOUT, ZERO_ENONFINITE):
+        return rc
+    _check(rc, "zero_plan_check")
 
 
 def zero_debug_drop_copy(tile):

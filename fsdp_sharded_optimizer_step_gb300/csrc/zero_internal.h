@@ -66,6 +66,7 @@ struct zero_plan {
     float *d_coef = nullptr;        // clip coefficient of the last clipped step
     int *d_err = nullptr;           // device error word: non-zero after a bounded wait expired
     unsigned long long *d_tickets = nullptr;  // [2]: segment tickets and finished CTAs of a pipelined launch
+    int *d_skipped = nullptr;       // non-zero after a clipped step found a non-finite norm (zero_plan_check)
     zero::UnitDesc *d_units = nullptr;  // device unit table
 };
 

@@ -895,7 +895,8 @@ __device__ __forceinline__ double block_sum(double x, double *smem) {
 // rounded once to binary32 (NaN when S is not finite: the update then skips).
 constexpr int kFinThreads = 1024;
 __global__ void __launch_bounds__(kFinThreads) k_finalize(const double *partials, int64_t nseg, float max_norm,
-                                                          double *sqnorm_ws, double *sqnorm_out, float *coef_out) {
+                                                          double *sqnorm_ws, double *sqnorm_out, float *coef_out,
+                                                          int *skipped) {
     __shared__ double smem[kFinThreads / 32];
     double s = 0.0;
     for (int64_t i = threadIdx.x; i < nseg; i += kFinThreads) s = __dadd_rn(s, partials[i]);
@@ -907,6 +908,7 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(const double *partials
             float coef;
             if (!isfinite(S)) {
                 coef = __int_as_float(0x7FC00000);
+                *skipped = 1;
             } else {
                 double c = __ddiv_rn(static_cast<double>(max_norm), __dadd_rn(__dsqrt_rn(S), 1e-6));
                 if (c > 1.0) c = 1.0;
@@ -1040,6 +1042,9 @@ static bool valid_dtype(int32_t d) { return d == ZERO_BF16 || d == ZERO_F32; }
 #ifndef ZERO_PIPE_SMEM_BUDGET
 #define ZERO_PIPE_SMEM_BUDGET (200 * 1024)
 #endif
+#ifndef ZERO_PIPE_MIN_STAGES
+#define ZERO_PIPE_MIN_STAGES 2
+#endif
 #ifndef ZERO_PIPE_STAGE_TARGET
 #define ZERO_PIPE_STAGE_TARGET (64 * 1024)
 #endif
@@ -1051,15 +1056,18 @@ struct PipeGeometry {
 };
 
 // Tile: a multiple of the consumers' pass width (4 elements per consumer
-// thread) close to ZERO_PIPE_STAGE_TARGET bytes per stage, halved while two
-// stages would not fit the shared-memory budget; then as many stages as fit.
+// thread) close to ZERO_PIPE_STAGE_TARGET bytes per stage, halved while
+// ZERO_PIPE_MIN_STAGES stages would not fit the shared-memory budget; then as
+// many stages as fit.  (A tile below the pass width leaves some consumer
+// threads without work in a pass; the loop allows any multiple of 8.)
 static PipeGeometry pipe_geometry(int mode, int n_ranks, int gdtype) {
     const int gb = gdtype == ZERO_BF16 ? 2 : 4;
     const size_t per_elem = mode == MODE_SHARD ? 16 : static_cast<size_t>(n_ranks) * gb + (mode == MODE_FUSED ? 12 : 0);
     const size_t quantum = 4 * kConsumerWarps * 32;
     const size_t mult = ZERO_PIPE_STAGE_TARGET / (quantum * per_elem);
     int tile = static_cast<int>(quantum * (mult > 0 ? mult : 1));
-    while (tile > 64 && 2 * static_cast<size_t>(stage_layout(mode, n_ranks, gb, tile).bytes) > ZERO_PIPE_SMEM_BUDGET)
+    while (tile > 64 && static_cast<size_t>(ZERO_PIPE_MIN_STAGES) * stage_layout(mode, n_ranks, gb, tile).bytes >
+                            ZERO_PIPE_SMEM_BUDGET)
         tile >>= 1;
     const size_t stage_bytes = stage_layout(mode, n_ranks, gb, tile).bytes;
     int stages = static_cast<int>(ZERO_PIPE_SMEM_BUDGET / stage_bytes);
@@ -1161,6 +1169,7 @@ extern "C" int zero_plan_attach(zero_plan *plan, void *workspace, size_t bytes, 
     plan->d_coef = reinterpret_cast<float *>(base + L.scalars + 8);
     plan->d_err = reinterpret_cast<int *>(base + L.scalars + 16);
     plan->d_tickets = reinterpret_cast<unsigned long long *>(base + L.scalars + 24);
+    plan->d_skipped = reinterpret_cast<int *>(base + L.scalars + 40);
     if (!plan->unit_table.empty()) {
         e = cudaMemcpyAsync(base + L.units, plan->unit_table.data(), plan->unit_table.size() * sizeof(UnitDesc),
                             cudaMemcpyHostToDevice, reinterpret_cast<cudaStream_t>(stream));
@@ -1209,7 +1218,8 @@ static int launch_norm(const zero_plan *plan, const void *const *grads, int32_t 
     const int64_t nseg = static_cast<int64_t>(plan->segs.size());
     const int rc = launch_pipe(MODE_REDUCE, gdtype, nseg, kp, st);
     if (rc != ZERO_OK) return rc;
-    k_finalize<<<1, kFinThreads, 0, st>>>(plan->d_partials, nseg, max_norm, plan->d_sqnorm, sqnorm_out, plan->d_coef);
+    k_finalize<<<1, kFinThreads, 0, st>>>(plan->d_partials, nseg, max_norm, plan->d_sqnorm, sqnorm_out, plan->d_coef,
+                                          plan->d_skipped);
     return launch_status();
 }
 
@@ -1391,6 +1401,22 @@ extern "C" int zero_reduce_scatter_unit(const zero_plan *plan, int32_t unit, con
 extern "C" int zero_debug_drop_copy(int64_t tile) {
     if (tile < -1) return ZERO_EINVAL;
     g_drop_tile.store(tile);
+    return ZERO_OK;
+}
+
+extern "C" int zero_plan_check(const zero_plan *plan, zero_stream_t stream) {
+    int rc = check_attached(plan);
+    if (rc != ZERO_OK) return rc;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int32_t err = 0, skipped = 0;
+    cudaError_t e = cudaMemcpyAsync(&err, plan->d_err, sizeof(err), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&skipped, plan->d_skipped, sizeof(skipped), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(plan->d_err, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(plan->d_skipped, 0, sizeof(int32_t), st);
+    if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
+    if (err != 0) return ZERO_ETIMEOUT;
+    if (skipped != 0) return ZERO_ENONFINITE;
     return ZERO_OK;
 }
 

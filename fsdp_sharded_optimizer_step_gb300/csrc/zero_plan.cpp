@@ -190,6 +190,8 @@ extern "C" const char *zero_status_string(int status) {
         case ZERO_ENOMEM: return "out of memory (host) or workspace too small";
         case ZERO_ECUDA: return "CUDA runtime error";
         case ZERO_EALIGN: return "device pointer not 16-byte aligned";
+        case ZERO_ENONFINITE: return "a clipped step was skipped: the global gradient norm was not finite";
+        case ZERO_ETIMEOUT: return "a bounded wait inside a kernel expired: that work is incomplete";
         case ZERO_ENOTATTACHED: return "plan has no device workspace (call zero_plan_attach)";
         case ZERO_ERANGE: return "size beyond the fixed capacity of the allocation-free entry point";
         default: return "unknown status";

@@ -87,6 +87,8 @@ enum {
     ZERO_ENOMEM = -2,      /* host allocation failed, or the workspace is too small */
     ZERO_ECUDA = -3,       /* a CUDA runtime call failed (launch, copy, device query) */
     ZERO_EALIGN = -4,      /* a device pointer is not 16-byte aligned */
+    ZERO_ENONFINITE = -5,  /* zero_plan_check: a clipped step was skipped, its global norm was inf/NaN */
+    ZERO_ETIMEOUT = -6,    /* zero_plan_check: a bounded wait inside a kernel expired */
     ZERO_ENOTATTACHED = -7, /* the plan has no device workspace yet (zero_plan_attach) */
     ZERO_ERANGE = -8        /* a size beyond a fixed capacity (zero_grad_sqnorm_noalloc) */
 };
@@ -308,6 +310,17 @@ int zero_grad_sqnorm_noalloc(const void *const *grads, int32_t n_ranks, int32_t 
  * when one gave up (the step it belonged to stopped early and its results are
  * incomplete).  No kernel waits longer than about two seconds. */
 int zero_plan_device_errors(const zero_plan *plan, zero_stream_t stream, int32_t *errors);
+
+/* The outcome of the device work enqueued on the plan since the previous
+ * check, as a status; synchronises `stream`.  Device calls return as soon as
+ * their kernels are queued, so conditions found on the device are reported
+ * here: ZERO_ETIMEOUT when a bounded wait expired (that work is incomplete,
+ * as for zero_plan_device_errors), else ZERO_ENONFINITE when a clipped
+ * zero_step found a non-finite global norm and left master, m, v and the
+ * params untouched (the pages leave that case open; skipping the step is the
+ * reading taken), else ZERO_OK.  Both conditions are cleared.  ZERO_EINVAL /
+ * ZERO_ENOTATTACHED / ZERO_ECUDA as usual. */
+int zero_plan_check(const zero_plan *plan, zero_stream_t stream);
 
 /* Testing aid for the bounded waits (failure detection without a GPU fault):
  * arms the NEXT pipelined launch so that the copies of tile number `tile`

@@ -143,8 +143,12 @@ def test_argument_errors_are_reported_on_the_host(zlib):
     assert L.zero_bias_corrections(0, C.c_float(0.9), C.c_float(0.95), C.byref(C.c_float()), C.byref(C.c_float())) \
         == B.ZERO_EINVAL
     assert L.zero_plan_query(None, None, None, None, None, None, None) == B.ZERO_EINVAL
-    for s in (0, -1, -2, -3, -4, -7, -99):
+    for s in (0, -1, -2, -3, -4, -5, -6, -7, -8, -99):
         assert len(L.zero_status_string(s)) > 0
+    for s in (-5, -6):  # the statuses zero_plan_check reports have their own text
+        assert L.zero_status_string(s) != L.zero_status_string(-99)
+    assert L.zero_plan_check(h, None) == B.ZERO_ENOTATTACHED
+    assert L.zero_plan_check(None, None) == B.ZERO_EINVAL
     L.zero_plan_destroy(h)
     L.zero_plan_destroy(None)
 

@@ -318,6 +318,9 @@ def test_clipped_step_skipped_when_norm_not_finite():
     assert math.isinf(c.sq.item())
     for x, y in zip(before, (c.master, c.m, c.v, c.full, c.pshard)):
         assert torch.equal(host_bits_t(x), host_bits_t(y))
+    from fsdp_sharded_optimizer_step_gb300 import binding as B
+    assert Z.zero_plan_check(c.plan) == B.ZERO_ENONFINITE  # reported on the host, then cleared
+    assert Z.zero_plan_check(c.plan) == B.ZERO_OK
     c.g_o = oracle_grad_rows(c.grads)
     assert c.oracle_step(1, max_norm=1.0) == O.ENONFINITE
 
@@ -489,6 +492,10 @@ def test_bounded_wait_runs_out_and_is_reported():
     assert B.zero_plan_device_errors(c.plan) != 0
     assert 1.5 < elapsed < 30.0
     assert B.zero_plan_device_errors(c.plan) == 0  # read-and-clear
+    B.zero_debug_drop_copy(3)  # the same, reported as a status
+    c.gpu_step(2)
+    assert Z.zero_plan_check(c.plan) == B.ZERO_ETIMEOUT
+    assert Z.zero_plan_check(c.plan) == B.ZERO_OK
     d = SmallCase([70001, 3000], 8, W.BF16, W.BF16, seed=52)
     d.gpu_step(1)
     assert d.oracle_step(1) == O.OK
