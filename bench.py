@@ -289,17 +289,22 @@ def measure_e2e(args, world, dev, stream, grads, full, step, N, P, gdt, pdt, psi
         e2e_step(10_000 + t)
     torch.cuda.synchronize(dev)
     barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
+    marks[0].record(stream)
     for k in range(e2e_steps):
         e2e_step(20_000 + k)
-    e1.record(stream)
+        marks[k + 1].record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    per_step = [marks[k].elapsed_time(marks[k + 1]) for k in range(e2e_steps)]
+    e2e_ms = max_over_ranks(marks[0].elapsed_time(marks[-1]) / e2e_steps, world, dev)
+    h2d = h_grads.numel() * h_grads.element_size()
+    d2h = h_full.numel() * h_full.element_size()
     e2e = {"value": world * psi / (e2e_ms / 1e3), "unit": UNIT,
-           "h2d_bytes_per_step": h_grads.numel() * h_grads.element_size(),
-           "d2h_bytes_per_step": h_full.numel() * h_full.element_size(), "ms_per_step": e2e_ms, "steps": e2e_steps,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps,
+           # the host link's speed varies from step to step: the per-step spread, and the link rate
+           # the fastest step reached (all copied bytes over its time)
+           "median_ms": statistics.median(per_step), "min_ms": min(per_step), "max_ms": max(per_step),
+           "link_GBs_at_min": (h2d + d2h) / (min(per_step) / 1e3) / 1e9,
            "mode": "streamed per unit: copy-in, update and copy-out overlapped" if streamed
            else "copy all gradients in, step, copy params out"}
     del h_grads, h_full

@@ -930,31 +930,43 @@ __global__ void __launch_bounds__(kThreads) k_gather(const KParams p) {
     // destination element 0 is full position g_origin (0, or F_u for a unit-sized destination);
     // sp.gvec is the alignment relative to that origin
     char *dst = static_cast<char *>(p.full) + (sg.g_off - p.g_origin) * esz;
-    for (int i = threadIdx.x; i < sp.ngroups; i += kThreads) {
+    int i = threadIdx.x;
+    if (sp.gvec) {
+        // aligned like the shard: whole 16-byte vectors, four groups per thread in flight
+        // (one group = 8 elements = 1 vector for bf16, 2 for fp32)
+        const int vpg = esz / 2;  // vectors per group
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(src + sp.k0 * esz);
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst + sp.k0 * esz);
+        const int nv = sp.ngroups * vpg;
+        int v = threadIdx.x;
+        for (; v + 3 * kThreads < nv; v += 4 * kThreads) {
+            const uint4 x0 = __ldcs(s4 + v), x1 = __ldcs(s4 + v + kThreads);
+            const uint4 x2 = __ldcs(s4 + v + 2 * kThreads), x3 = __ldcs(s4 + v + 3 * kThreads);
+            __stcs(d4 + v, x0);
+            __stcs(d4 + v + kThreads, x1);
+            __stcs(d4 + v + 2 * kThreads, x2);
+            __stcs(d4 + v + 3 * kThreads, x3);
+        }
+        for (; v < nv; v += kThreads) __stcs(d4 + v, __ldcs(s4 + v));
+        i = sp.ngroups;  // no groups left for the loop below
+    }
+    for (; i < sp.ngroups; i += kThreads) {  // destination not aligned like the shard: element stores
         const int k = sp.k0 + 8 * i;
         if (esz == 2) {
             const uint4 x = __ldcs(reinterpret_cast<const uint4 *>(src + k * 2));
-            if (sp.gvec) {
-                __stcs(reinterpret_cast<uint4 *>(dst + k * 2), x);
-            } else {
-                unsigned short *d = reinterpret_cast<unsigned short *>(dst) + k;
-                const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+            unsigned short *d = reinterpret_cast<unsigned short *>(dst) + k;
+            const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    d[2 * e] = static_cast<unsigned short>(w4[e] & 0xFFFFu);
-                    d[2 * e + 1] = static_cast<unsigned short>(w4[e] >> 16);
-                }
+            for (int e = 0; e < 4; ++e) {
+                d[2 * e] = static_cast<unsigned short>(w4[e] & 0xFFFFu);
+                d[2 * e + 1] = static_cast<unsigned short>(w4[e] >> 16);
             }
         } else {
             float x[8];
             load8(reinterpret_cast<const float *>(src) + k, x);
             float *d = reinterpret_cast<float *>(dst) + k;
-            if (sp.gvec) {
-                store8(d, x);
-            } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) d[e] = x[e];
-            }
+            for (int e = 0; e < 8; ++e) d[e] = x[e];
         }
     }
     const int nedge = sp.k0 + (sg.len - sp.tail0);
