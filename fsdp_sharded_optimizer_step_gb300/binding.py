@@ -237,6 +237,18 @@ def rank_buffers(n_ranks, length, dtype, device, zero=False):
 # ------------------------------------------------------------------ tensor marshalling
 def _rows(plan, x, length, what, dtypes):
     """A [N, length] tensor or a list of N 1-D tensors -> host array of N device pointers, dtype code."""
+    if isinstance(x, torch.Tensor) and x.dim() == 2:
+        # rows of one 2-D tensor: pointers from its row stride, no per-row tensor objects
+        if x.shape[0] != plan.n_ranks:
+            raise ValueError(f"{what}: expected {plan.n_ranks} rank buffers, got {x.shape[0]}")
+        if x.device != plan.device:
+            raise ValueError(f"{what}: tensor on {x.device}, plan on {plan.device}")
+        if x.dtype not in dtypes:
+            raise ValueError(f"{what}: dtype {x.dtype} not allowed")
+        if x.shape[1] != length or (length > 1 and x.stride(1) != 1):
+            raise ValueError(f"{what}: each rank buffer must be contiguous 1-D of {length} elements")
+        base, step = x.data_ptr(), x.stride(0) * x.element_size()
+        return (C.c_void_p * plan.n_ranks)(*[base + r * step for r in range(plan.n_ranks)]), _DTYPES[x.dtype]
     rows = list(x.unbind(0)) if isinstance(x, torch.Tensor) else list(x)
     if len(rows) != plan.n_ranks:
         raise ValueError(f"{what}: expected {plan.n_ranks} rank buffers, got {len(rows)}")
