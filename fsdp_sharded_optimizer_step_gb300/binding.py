@@ -247,6 +247,8 @@ def _rows(plan, x, length, what, dtypes):
             raise ValueError(f"{what}: dtype {x.dtype} not allowed")
         if x.shape[1] != length or (length > 1 and x.stride(1) != 1):
             raise ValueError(f"{what}: each rank buffer must be contiguous 1-D of {length} elements")
+        if length == 0:  # nothing to address: null pointers, as for empty rows below
+            return (C.c_void_p * plan.n_ranks)(), _DTYPES[x.dtype]
         base, step = x.data_ptr(), x.stride(0) * x.element_size()
         return (C.c_void_p * plan.n_ranks)(*[base + r * step for r in range(plan.n_ranks)]), _DTYPES[x.dtype]
     rows = list(x.unbind(0)) if isinstance(x, torch.Tensor) else list(x)

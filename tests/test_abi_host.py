@@ -159,3 +159,26 @@ def test_binding_refuses_wrong_tensors_on_the_host(zlib):
     with pytest.raises(ValueError):
         Z.zero_reduce_scatter(p, torch.zeros(2, p.P_pad, dtype=torch.bfloat16),
                               torch.zeros(2, p.H, dtype=torch.float32))
+
+
+def test_rank_pointers_of_a_2d_tensor_match_its_rows():
+    """The binding takes the N rank pointers of a [N, L] tensor from its row stride;
+    they must be the pointers of its rows (padded rows, views, empty buffers)."""
+    import torch
+
+    class Plan:
+        n_ranks = 4
+        device = torch.device("cpu")
+
+    for x in (torch.zeros(4, 1000, dtype=torch.bfloat16), torch.zeros(4, 1008, dtype=torch.float32)[:, :1000],
+              torch.zeros(5, 1000, dtype=torch.bfloat16)[1:], torch.zeros(4, 0, dtype=torch.bfloat16)):
+        L = x.shape[1]
+        fast, dt = B._rows(Plan, x, L, "x", B._G)
+        rows, dt2 = B._rows(Plan, list(x.unbind(0)), L, "x", B._G)
+        assert dt == dt2 and [fast[i] for i in range(4)] == [rows[i] for i in range(4)]
+    with pytest.raises(ValueError):
+        B._rows(Plan, torch.zeros(4, 10, dtype=torch.bfloat16)[:, ::2], 5, "x", B._G)  # rows not contiguous
+    with pytest.raises(ValueError):
+        B._rows(Plan, torch.zeros(3, 10, dtype=torch.bfloat16), 10, "x", B._G)  # wrong rank count
+    with pytest.raises(ValueError):
+        B._rows(Plan, torch.zeros(4, 10, dtype=torch.float16), 10, "x", B._G)  # dtype
