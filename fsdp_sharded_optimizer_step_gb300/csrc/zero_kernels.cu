@@ -1057,6 +1057,9 @@ static bool valid_dtype(int32_t d) { return d == ZERO_BF16 || d == ZERO_F32; }
 #ifndef ZERO_PIPE_MIN_STAGES
 #define ZERO_PIPE_MIN_STAGES 2
 #endif
+#ifndef ZERO_PIPE_TILE_STEP
+#define ZERO_PIPE_TILE_STEP 0  // 0: halve the tile while the stages do not fit; else shrink it by this many elements
+#endif
 #ifndef ZERO_PIPE_STAGE_TARGET
 #define ZERO_PIPE_STAGE_TARGET (64 * 1024)
 #endif
@@ -1068,7 +1071,7 @@ struct PipeGeometry {
 };
 
 // Tile: a multiple of the consumers' pass width (4 elements per consumer
-// thread) close to ZERO_PIPE_STAGE_TARGET bytes per stage, halved while
+// thread) close to ZERO_PIPE_STAGE_TARGET bytes per stage, reduced while
 // ZERO_PIPE_MIN_STAGES stages would not fit the shared-memory budget; then as
 // many stages as fit.  (A tile below the pass width leaves some consumer
 // threads without work in a pass; the loop allows any multiple of 8.)
@@ -1080,7 +1083,7 @@ static PipeGeometry pipe_geometry(int mode, int n_ranks, int gdtype) {
     int tile = static_cast<int>(quantum * (mult > 0 ? mult : 1));
     while (tile > 64 && static_cast<size_t>(ZERO_PIPE_MIN_STAGES) * stage_layout(mode, n_ranks, gb, tile).bytes >
                             ZERO_PIPE_SMEM_BUDGET)
-        tile >>= 1;
+        tile = (ZERO_PIPE_TILE_STEP > 0 && tile > 2 * ZERO_PIPE_TILE_STEP) ? tile - ZERO_PIPE_TILE_STEP : tile >> 1;
     const size_t stage_bytes = stage_layout(mode, n_ranks, gb, tile).bytes;
     int stages = static_cast<int>(ZERO_PIPE_SMEM_BUDGET / stage_bytes);
     if (stages > kMaxStages) stages = kMaxStages;
