@@ -34,12 +34,17 @@ sys.path.insert(0, ROOT)
 METRIC = "sharded-step params/sec and achieved HBM GB/s (% of GB300 peak) at 1 GPU"
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRC = os.path.join(ROOT, "fsdp_sharded_optimizer_step_gb300", "csrc", "zero_kernels.cu")
+KERNEL_SRC = [os.path.join(ROOT, "fsdp_sharded_optimizer_step_gb300", "csrc", f)
+              for f in ("zero_kernels.cu", "zero_internal.h")]
 
 
 def kernel_source_hash():
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """First 16 hex digits of the SHA-256 of the kernels' source and the structs they use."""
+    h = hashlib.sha256()
+    for path in KERNEL_SRC:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def measured_hbm_peak():
