@@ -79,6 +79,10 @@ CONFIGS = {
                             "84,006,400 params), N=8, bf16 grads N(0,1e-3); 3.5 GB of traffic per step",
                        units=lambda: gpt2l_units()[:2], N=8, gdtype=BF16, pdtype=BF16, stage=1, steps=3, max_norm=0.0,
                        grad_sigma=1e-3, master_sigma=0.02),
+    "1p3b_clip_prof": dict(desc="profiling case: two 1.3B blocks (100,716,544 params), N=8, clip 1.0, bf16 grads "
+                                "N(0,1e-2) with 0.1% outliers x100; about 3.5 GB resident",
+                           units=lambda: gpt_1p3b_units()[1:3], N=8, gdtype=BF16, pdtype=BF16, stage=2, steps=3,
+                           max_norm=1.0, grad_sigma=1e-2, outlier_frac=1e-3, outlier_scale=100.0, master_sigma=0.02),
     "finewrap_prof": dict(desc="profiling case: 128 fine-wrap units (same law, seed 4), N=16, bf16 grads "
                                "N(0,1e-3); about 3 GB resident",
                           units=lambda: finewrap_units(n_units=128), N=16, gdtype=BF16, pdtype=BF16, stage=2, steps=3,
