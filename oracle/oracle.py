@@ -48,6 +48,7 @@ def lib():
             "orc_sqacc_bytes": (i32, []),
             "orc_sqacc_add_square": (None, [p, f32]),
             "orc_sqacc_result": (f64, [p]),
+            "orc_sqacc_merge": (None, [p, p]),
             "orc_sqnorm_accumulate": (C.c_int, [p, i64, i32, p, i32, p]),
             "orc_clip_coef": (f32, [f64, f32]),
             "orc_adamw": (C.c_int, [i64, i32, p, i32, p, p, p, p, p, i32, p, i32, f32]),
@@ -159,6 +160,10 @@ class SqAcc:
         n = grads[0].size
         arr = (C.c_void_p * len(grads))(*[g.ctypes.data for g in grads])
         _check(lib().orc_sqnorm_accumulate(self.buf, n, len(grads), arr, gdtype, _ptr(pad)), "sqnorm")
+
+    def merge(self, other: "SqAcc"):
+        """Adds another accumulator's exact sum into this one."""
+        lib().orc_sqacc_merge(self.buf, other.buf)
 
     def result(self) -> float:
         return lib().orc_sqacc_result(self.buf)

@@ -310,6 +310,21 @@ void orc_sqacc_add_square(orc_sqacc *a, float g)
     }
 }
 
+/* dst += src, exactly (limb-wise addition with carry), so that partial sums of
+ * squares taken over disjoint sets of positions combine into the same exact
+ * value as one pass over all of them. */
+void orc_sqacc_merge(orc_sqacc *dst, const orc_sqacc *src)
+{
+    uint64_t carry = 0u;
+    for (int k = 0; k < ORC_ACC_LIMBS; ++k) {
+        unsigned __int128 t = (unsigned __int128)dst->limb[k] + src->limb[k] + carry;
+        dst->limb[k] = (uint64_t)t;
+        carry = (uint64_t)(t >> 64);
+    }
+    dst->nan_seen |= src->nan_seen;
+    dst->inf_seen |= src->inf_seen;
+}
+
 static int orc_bitlen128(unsigned __int128 x)
 {
     int n = 0;

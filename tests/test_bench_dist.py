@@ -66,3 +66,44 @@ def test_reference_arm_under_torchrun_world_2():
     lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1  # rank 0 only
     _check_reference_line(lines[0], 2)
+
+
+def test_all_cores_oracle_step_is_bit_identical_to_the_oracle_step():
+    """The bench's all-cores CPU row runs the oracle's functions on one chunk of
+    positions per thread (clip: exact partial sums of squares merged); w, m, v, the
+    output and S must equal one single-threaded oracle step bit for bit."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    from oracle import build as obuild
+    from oracle import oracle as O
+    obuild.build()
+    rng = np.random.default_rng(3)
+    n, N = 100_003, 8
+    for gd, max_norm in ((O.BF16, 0.0), (O.BF16, 1e-3), (O.F32, 0.5), (O.F32, 0.0)):
+        g = (rng.normal(0, 1e-2, (N, n))).astype(np.float32)
+        rows = [(r.view(np.uint32) >> 16).astype(np.uint16) for r in g] if gd == O.BF16 else list(g)
+        w0 = rng.normal(0, 0.02, n).astype(np.float32)
+        m0 = (rng.normal(0, 1e-3, n)).astype(np.float32)
+        v0 = (rng.random(n) * 1e-6).astype(np.float32)
+        hp = O.hparams(t=3, max_norm=max_norm)
+        w1, m1, v1 = w0.copy(), m0.copy(), v0.copy()
+        rc1, out1, S1 = O.step(rows, gd, w1, m1, v1, hp, pdtype=O.BF16)
+        w2, m2, v2 = w0.copy(), m0.copy(), v0.copy()
+        with ThreadPoolExecutor(7) as ex:
+            rc2, out2, S2 = bench.oracle_step_all_cores(ex, 7, rows, gd, w2, m2, v2, hp, O.BF16, max_norm)
+        assert rc1 == rc2 == O.OK
+        for a, b in ((w1, w2), (m1, m2), (v1, v2)):
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+        assert np.array_equal(out1, out2)
+        if max_norm > 0:
+            assert S1 == S2
+    # a non-finite norm: the step is skipped on both sides
+    rows = [np.full(10, np.inf, np.float32)] + [np.zeros(10, np.float32)] * 3
+    w = np.zeros(10, np.float32)
+    with ThreadPoolExecutor(3) as ex:
+        rc, out, S = bench.oracle_step_all_cores(ex, 3, rows, O.F32, w, w.copy(), w.copy(),
+                                                 O.hparams(t=1, max_norm=1.0), O.BF16, 1.0)
+    assert rc == O.ENONFINITE and S == float("inf")

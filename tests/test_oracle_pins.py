@@ -315,6 +315,32 @@ def test_sqnorm_is_exact_sum_of_squares(orc):
     assert orc.sqnorm([x], orc.F32) == math.fsum(float(a) ** 2 for a in x.astype(np.float64))
 
 
+def test_sqnorm_partial_accumulators_merge_exactly(orc):
+    """Squares taken over disjoint chunks and merged give the one-pass S, which is
+    the exact rational sum rounded once (the accumulator is free of any order)."""
+    rng = np.random.default_rng(11)
+    x = (rng.normal(0, 1, 3000) * np.exp(rng.uniform(-60, 60, 3000))).astype(np.float32)
+    x[:40] = np.float32(3.0e38)  # carries across limbs
+    whole = orc.sqnorm([x], orc.F32)
+    assert whole == X.rn64(sum(Fraction(float(a)) ** 2 for a in x))
+    for trial in range(5):
+        cuts = np.sort(rng.choice(np.arange(1, x.size), 7, replace=False))
+        acc = orc.SqAcc()
+        for part in np.split(x, cuts):
+            a = orc.SqAcc()
+            a.add_avg_grad([part], orc.F32)
+            acc.merge(a)
+        assert acc.result() == whole, trial
+    a, b = orc.SqAcc(), orc.SqAcc()
+    a.add_avg_grad([x[:10]], orc.F32)
+    b.add_avg_grad([np.array([np.inf], np.float32)], orc.F32)
+    a.merge(b)
+    assert math.isinf(a.result())
+    b.add_avg_grad([np.array([np.nan], np.float32)], orc.F32)
+    a.merge(b)
+    assert math.isnan(a.result())
+
+
 def test_sqnorm_of_averaged_gradient_with_pads(orc):
     rng = np.random.default_rng(6)
     g = [rng.normal(0, 1, 64).astype(np.float32) for _ in range(4)]
