@@ -153,26 +153,37 @@ int orc_locate(const int64_t *sizes, int32_t n_units, int32_t n_ranks, int64_t n
                int32_t *rank, int64_t *shard_pos, uint8_t *is_pad)
 {
     if (n_units < 0 || n_ranks < 1 || n < 0) return ORC_EINVAL;
-    for (int64_t i = 0; i < n; ++i) {
-        int64_t f = 0, hh = 0;
-        int found = 0;
-        for (int32_t u = 0; u < n_units && !found; ++u) {
-            int64_t rem = sizes[u] % n_ranks;
-            int64_t Su = rem == 0 ? sizes[u] : sizes[u] + (n_ranks - rem);
-            int64_t hu = Su / n_ranks;
-            if (pos[i] >= f && pos[i] < f + Su) {
-                int64_t k = pos[i] - f;
-                rank[i] = (int32_t)(k / hu);
-                shard_pos[i] = hh + k % hu;
-                is_pad[i] = (uint8_t)(k >= sizes[u]);
-                found = 1;
-            }
-            f += Su;
-            hh += hu;
-        }
-        if (!found) return ORC_EINVAL;
+    /* the layout of every unit once: F (full offset), S (padded size), h (slice), Hoff */
+    int64_t *t = (int64_t *)malloc(sizeof(int64_t) * 4 * (size_t)(n_units > 0 ? n_units : 1));
+    if (t == NULL) return ORC_EINVAL;
+    int64_t f = 0, hh = 0;
+    for (int32_t u = 0; u < n_units; ++u) {
+        int64_t rem = sizes[u] % n_ranks;
+        int64_t Su = rem == 0 ? sizes[u] : sizes[u] + (n_ranks - rem);
+        t[4 * u] = f;
+        t[4 * u + 1] = Su;
+        t[4 * u + 2] = Su / n_ranks;
+        t[4 * u + 3] = hh;
+        f += Su;
+        hh += Su / n_ranks;
     }
-    return ORC_OK;
+    int rc = ORC_OK;
+    for (int64_t i = 0; i < n && rc == ORC_OK; ++i) {
+        /* the last unit whose offset F is <= pos (a unit of size 0 owns no position) */
+        int32_t lo = 0, hi = n_units - 1, u = -1;
+        while (lo <= hi) {
+            int32_t mid = lo + (hi - lo) / 2;
+            if (t[4 * mid] <= pos[i]) { u = mid; lo = mid + 1; } else { hi = mid - 1; }
+        }
+        while (u >= 0 && t[4 * u + 1] == 0) --u;
+        if (u < 0 || pos[i] < t[4 * u] || pos[i] >= t[4 * u] + t[4 * u + 1]) { rc = ORC_EINVAL; break; }
+        int64_t k = pos[i] - t[4 * u];
+        rank[i] = (int32_t)(k / t[4 * u + 2]);
+        shard_pos[i] = t[4 * u + 3] + k % t[4 * u + 2];
+        is_pad[i] = (uint8_t)(k >= sizes[u]);
+    }
+    free(t);
+    return rc;
 }
 
 /* ------------------------------------------------------------------------ */

@@ -384,7 +384,10 @@ def test_finewrap_full_size_sampled():
 
 @pytest.mark.slow
 def test_4b_zero3_full_size_sampled():
-    c = SampledCase("4b_z3", n_random=300000)
+    """4B ZeRO-3 (128 GB resident): 300k random positions, every slice boundary, and
+    every element of four whole 113M-parameter block units (first, second, a middle
+    one and the last block before the embedding)."""
+    c = SampledCase("4b_z3", n_random=300000, extra_units=(0, 1, 16, 31))
     c.gpu_step(1)
     c.assert_sample_equal(c.oracle_step(1))
 

@@ -459,6 +459,14 @@ def test_plan_brute_force(orc, N):
         for u in range(U):
             seg = pad[p.F[u]:p.F[u] + p.S[u]]
             assert np.array_equal(seg, (np.arange(p.S[u]) >= sizes[u]).astype(np.uint8))
+        # locate is the inverse of the shard map, with the pad flag of the position
+        if p.P_pad:
+            allpos = np.arange(p.P_pad, dtype=np.int64)
+            rank, spos, isp = p.locate(allpos[::-1].copy())
+            assert np.array_equal(mp[rank, spos], allpos[::-1])
+            assert np.array_equal(isp, pad[::-1])
+        with pytest.raises(RuntimeError):
+            p.locate(np.array([p.P_pad], np.int64))
 
 
 def test_plan_named_workloads(orc):
