@@ -32,6 +32,9 @@ MUTANTS = [
      "{ float q = orc_avg_grad(n_ranks, grads, gdtype, pad, i); orc_sqacc_add_square(a, sqrtf(q * q)); }"),
     ("clip_guard_dropped", "double c = (double)max_norm / (sqrt(S) + 1e-6);", "double c = (double)max_norm / sqrt(S);"),
     ("reshard_wrong_slice", "int64_t rs = k / h_from, js = k % h_from;", "int64_t rs = k / h_to, js = k % h_to;"),
+    ("locate_wrong_rank", "rank[i] = (int32_t)(k / t[4 * u + 2]);", "rank[i] = (int32_t)(k % n_ranks);"),
+    ("merge_drops_carry", "        dst->limb[k] = (uint64_t)t;\n        carry = (uint64_t)(t >> 64);",
+     "        dst->limb[k] = (uint64_t)t;\n        carry = 0u;"),
     ("toy_rank_slice", "float acc = c->slots[0][(int64_t)r * h + j];", "float acc = c->slots[0][(int64_t)r * h + j] * 0.5f;"),
 ]
 

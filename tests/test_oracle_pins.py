@@ -331,6 +331,13 @@ def test_sqnorm_partial_accumulators_merge_exactly(orc):
             a.add_avg_grad([part], orc.F32)
             acc.merge(a)
         assert acc.result() == whole, trial
+    # a carry out of a full limb: 2^21 squares of 1.0 fill half of one 64-bit limb, two halves overflow it
+    ones = np.ones(1 << 21, np.float32)
+    a, b = orc.SqAcc(), orc.SqAcc()
+    a.add_avg_grad([ones], orc.F32)
+    b.add_avg_grad([ones], orc.F32)
+    a.merge(b)
+    assert a.result() == float(1 << 22)
     a, b = orc.SqAcc(), orc.SqAcc()
     a.add_avg_grad([x[:10]], orc.F32)
     b.add_avg_grad([np.array([np.inf], np.float32)], orc.F32)
