@@ -61,16 +61,28 @@ def ncu_traffic(workload, kind="fused"):
     """DRAM bytes (read + write) of one step's update launch(es) from the committed
     ncu summary (kind "fused": the one fused launch; "clip": reduce + finalize +
     shard), or None when the summary is missing or the kernel changed since."""
-    path = os.path.join(ROOT, "profiles", f"k_pipe_{kind}_{workload}.md")
+    return _summary_traffic(f"k_pipe_{kind}_{workload}.md", kernel_source_hash())
+
+
+def _summary_traffic(name, source_hash):
     try:
-        text = open(path).read()
+        text = open(os.path.join(ROOT, "profiles", name)).read()
     except OSError:
         return None
     m = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
     t = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if not m or not t or m.group(1) != kernel_source_hash():
+    if not m or not t or m.group(1) != source_hash:
         return None
     return int(t.group(1))
+
+
+def reshard_source_hash():
+    """First 16 hex digits of the SHA-256 of the reshard kernel's source and the structs it uses."""
+    h = hashlib.sha256()
+    for f in ("zero_reshard.cu", "zero_internal.h"):
+        with open(os.path.join(ROOT, "fsdp_sharded_optimizer_step_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 # ------------------------------------------------------------------ clocks
@@ -409,6 +421,8 @@ def run_reshard(args, world, rank, local):
     nbytes = 3 * (pf.H * N * 4 + pt.H * N2 * 4)
     gbs = nbytes / (ms / 1e3) / 1e9
     peak, peak_kind = measured_hbm_peak()
+    per_launch = _summary_traffic(f"k_reshard_{args.config}_{N}to{N2}.md", reshard_source_hash())
+    traffic = None if per_launch is None else 3 * per_launch
     if rank == 0:
         print(json.dumps({"metric": "checkpoint reshard of master/m/v (GB/s of HBM traffic)", "value": world * gbs,
                           "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -417,7 +431,8 @@ def run_reshard(args, world, rank, local):
                           "config": {"workload": f"{args.config}: {cfg['desc']}", "from_ranks": N, "to_ranks": N2,
                                      "bytes_per_step": nbytes},
                           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
-                                       "frac": gbs / peak, "traffic": None, "peak_kind": peak_kind},
+                                       "frac": gbs / peak, "traffic": traffic, "peak_kind": peak_kind,
+                                       "per": "step (three launches, one per array)"},
                           "gpu_launches": 3 * args.steps}), flush=True)
     return 0
 
