@@ -35,7 +35,7 @@ METRIC = "sharded-step params/sec and achieved HBM GB/s (% of GB300 peak) at 1 G
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SRC = [os.path.join(ROOT, "fsdp_sharded_optimizer_step_gb300", "csrc", f)
-              for f in ("zero_kernels.cu", "zero_internal.h")]
+              for f in ("zero_kernels.cu", "zero_launch.h", "zero_internal.h")]
 
 
 def kernel_source_hash():

@@ -21,9 +21,9 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-prec-div=true"
               "-Xcompiler", "-fPIC,-ffp-contract=off,-O2", "-Xptxas", "-v"]
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-ffp-contract=off", "-fno-fast-math", "-Wall", "-Wextra"]
 
-SOURCES_CU = ["zero_kernels.cu", "zero_noalloc.cu", "zero_reshard.cu"]
+SOURCES_CU = ["zero_kernels.cu", "zero_abi.cu", "zero_noalloc.cu", "zero_reshard.cu"]
 SOURCES_CXX = ["zero_plan.cpp"]
-HEADERS = ["zero_internal.h"]
+HEADERS = ["zero_internal.h", "zero_launch.h"]
 
 
 def _newest_input():

@@ -1,13 +1,14 @@
-// Kernels of the sharded optimizer step for sm_103a, and the C-ABI entry
-// points that launch them.
+// The sm_103a kernels of the sharded optimizer step and their launch
+// functions (the interface in zero_launch.h; the C ABI is in zero_abi.cu).
 //
 // The path is element-wise and HBM-bound (no contraction, so no tensor
 // cores): per padded element the fused step reads N gradients plus master/m/v
-// and writes master/m/v plus the gathered param.  The kernels therefore aim
-// at bytes in flight: one CTA per launch-table segment, 256 threads, each
-// thread moving 8 consecutive elements per iteration with 16/32-byte vector
-// accesses (all N gradient rows loaded before the first add), streaming cache
-// hints on data touched once.
+// and writes master/m/v plus the gathered param.  k_pipe is a persistent,
+// warp-specialised kernel: per CTA one producer thread streams segment tiles
+// into a shared-memory ring with bulk copies while 16 consumer warps compute
+// from the ring, and segments are handed out dynamically from a ticket
+// counter.  k_finalize adds the clip's per-segment partial sums in a fixed
+// order; k_gather is the per-unit all-gather.
 //
 // Exactness: every float operation uses an explicit _rn intrinsic in the
 // order the header documents ("ZeRO and FSDP sharding", Code, AdamW::step),
@@ -18,7 +19,7 @@
 #include <cmath>
 #include <cstdint>
 
-#include "zero_internal.h"
+#include "zero_launch.h"
 
 namespace zero {
 
@@ -29,34 +30,6 @@ constexpr int kThreads = 256;
 constexpr int kConsumerWarps = ZERO_PIPE_CONSUMER_WARPS;
 constexpr int kPipeThreads = (kConsumerWarps + 1) * 32;
 constexpr int kSegRing = 8;  // segment numbers the producer may take ahead of its consumers
-
-struct KParams {
-    const Seg *segs;
-    int64_t seg_base;       // first segment of this launch
-    int32_t n_ranks;
-    int32_t pdtype;
-    int32_t pow2;           // N is a power of two: g = acc * inv_n is bit-identical to acc / N
-    float inv_n, nf;
-    AdamConsts c;
-    float coef;             // host clip coefficient (reduce-scatter); 1 = none
-    int32_t write_g, want_partials, use_coef_dev;
-    double *partials;       // per segment, indexed by absolute segment number
-    int *err;               // device error word (a bounded wait expired)
-    int32_t tile, stages;   // pipeline geometry of k_pipe
-    int64_t p_pad, h_len;   // element counts of full-length and shard buffers
-    int64_t g_origin;       // full position of element 0 of each gradient row (0, or F_u for unit-local rows)
-    int64_t g_len;          // elements in each gradient row (P_pad, or S_u for unit-local rows)
-    int64_t drop_tile;      // testing aid: the copies of this tile of segment 0 are skipped (-1: none)
-    unsigned long long *tickets;  // k_pipe's schedule: [0] next segment ticket, [1] CTAs done (0, 0 between launches)
-    const float *coef_dev;  // device clip coefficient (NaN: skip the step)
-    void *full;
-    const void *grads[ZERO_MAX_RANKS];
-    float *master[ZERO_MAX_RANKS];
-    float *m[ZERO_MAX_RANKS];
-    float *v[ZERO_MAX_RANKS];
-    void *pshard[ZERO_MAX_RANKS];
-    float *gshard[ZERO_MAX_RANKS];
-};
 
 // Diagnostic build (-DZERO_SELFCHECK): every shared/global access of the
 // pipeline is checked against its buffer and alignment first; a failed check
@@ -261,13 +234,7 @@ __device__ __forceinline__ SegSplit split_segment(const Seg &sg, int64_t g_origi
     return s;
 }
 
-// ------------------------------------------------------------------ the three update modes
-// MODE_FUSED:  N gradient rows + master/m/v -> master/m/v + params (one pass)
-// MODE_REDUCE: N gradient rows -> fp32 gradient shard and/or per-segment
-//              binary64 sums of squares of the averaged gradient
-// MODE_SHARD:  fp32 gradient shard (x device clip coefficient) + master/m/v
-//              -> master/m/v + params
-enum { MODE_FUSED = 0, MODE_REDUCE = 1, MODE_SHARD = 2 };
+// ------------------------------------------------------------------ the update modes (MODE_* in zero_launch.h)
 
 // Per-thread sum of squares without binary64 arithmetic per element (the
 // binary64 rate of this GPU is a small fraction of its binary32 rate): each
@@ -977,78 +944,12 @@ __global__ void __launch_bounds__(kThreads) k_gather(const KParams p) {
     }
 }
 
-// ------------------------------------------------------------------ host helpers
-static bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
-
-// A plan without elements (P_pad == 0) accepts null rank pointers: nothing is
-// ever read or written through them.
-static int check_rank_ptrs(const zero_plan *plan, const void *const *arr, bool required) {
-    if (arr == nullptr) return required ? ZERO_EINVAL : ZERO_OK;
-    for (int q = 0; q < plan->n_ranks; ++q) {
-        if (arr[q] == nullptr) {
-            if (plan->p_pad == 0) continue;
-            return ZERO_EINVAL;
-        }
-        if (!aligned16(arr[q])) return ZERO_EALIGN;
-    }
-    return ZERO_OK;
-}
-
-static int check_ptr(const zero_plan *plan, const void *ptr, bool required) {
-    if (ptr == nullptr) return (required && plan->p_pad != 0) ? ZERO_EINVAL : ZERO_OK;
-    return aligned16(ptr) ? ZERO_OK : ZERO_EALIGN;
-}
-
-static int check_attached(const zero_plan *plan) {
-    if (plan == nullptr) return ZERO_EINVAL;
-    if (!plan->attached) return ZERO_ENOTATTACHED;
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
-    if (dev != plan->device) return ZERO_EINVAL;
-    return ZERO_OK;
-}
-
-static void fill_common(const zero_plan *plan, KParams &kp) {
-    kp = KParams{};
-    kp.segs = plan->d_segs;
-    kp.n_ranks = plan->n_ranks;
-    const int n = plan->n_ranks;
-    kp.pow2 = (n & (n - 1)) == 0;
-    kp.nf = static_cast<float>(n);
-    kp.inv_n = kp.pow2 ? 1.0f / static_cast<float>(n) : 0.0f;  // exact for a power of two
-    kp.coef = 1.0f;
-    kp.partials = plan->d_partials;
-    kp.err = plan->d_err;
-    kp.p_pad = plan->p_pad;
-    kp.h_len = plan->H;
-    kp.g_origin = 0;
-    kp.g_len = plan->p_pad;
-    kp.drop_tile = -1;
-    kp.tickets = plan->d_tickets;
-}
-
-static int launch_status() {
+// ------------------------------------------------------------------ launch status
+int launch_status() {
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
     return ZERO_OK;
 }
-
-// Segment range of one unit, or of all units.
-static int seg_range(const zero_plan *plan, int32_t unit, int64_t &begin, int64_t &count) {
-    if (unit < -1 || unit >= plan->n_units) return ZERO_EINVAL;
-    if (unit == -1) {
-        begin = 0;
-        count = static_cast<int64_t>(plan->segs.size());
-    } else {
-        begin = plan->unit_seg_begin[unit];
-        count = plan->unit_seg_begin[unit + 1] - begin;
-    }
-    if (count > 0x7FFFFFFF) return ZERO_EINVAL;
-    return ZERO_OK;
-}
-
-static bool valid_dtype(int32_t d) { return d == ZERO_BF16 || d == ZERO_F32; }
 
 // ------------------------------------------------------------------ pipeline geometry and launch
 #ifndef ZERO_PIPE_SMEM_BUDGET
@@ -1146,7 +1047,7 @@ static int launch_pipe_mode(int gd, int nr, int64_t nseg, const KParams &kp, con
 static std::atomic<int64_t> g_drop_tile{-1};
 
 // One launch of the pipeline in `mode` over segments [kp.seg_base, kp.seg_base + nseg).
-static int launch_pipe(int mode, int gd, int64_t nseg, KParams &kp, cudaStream_t st) {
+int launch_pipe(int mode, int gd, int64_t nseg, KParams &kp, cudaStream_t st) {
     if (nseg <= 0) return ZERO_OK;
     kp.drop_tile = g_drop_tile.exchange(-1);
     const PipeGeometry g = pipe_geometry(mode, kp.n_ranks, gd);
@@ -1159,292 +1060,18 @@ static int launch_pipe(int mode, int gd, int64_t nseg, KParams &kp, cudaStream_t
     }
 }
 
+void arm_drop_tile(int64_t tile) { g_drop_tile.store(tile); }
+
+int launch_finalize(const double *partials, int64_t nseg, float max_norm, double *sqnorm_ws, double *sqnorm_out,
+                    float *coef_out, int *skipped, cudaStream_t st) {
+    k_finalize<<<1, kFinThreads, 0, st>>>(partials, nseg, max_norm, sqnorm_ws, sqnorm_out, coef_out, skipped);
+    return launch_status();
+}
+
+int launch_gather(int64_t count, const KParams &kp, cudaStream_t st) {
+    if (count <= 0) return ZERO_OK;
+    k_gather<<<static_cast<unsigned>(count), kThreads, 0, st>>>(kp);
+    return launch_status();
+}
+
 }  // namespace zero
-
-using namespace zero;
-
-// ------------------------------------------------------------------ C ABI
-extern "C" int zero_plan_attach(zero_plan *plan, void *workspace, size_t bytes, zero_stream_t stream) {
-    if (plan == nullptr || workspace == nullptr || plan->attached) return ZERO_EINVAL;
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ZERO_EALIGN;
-    const WsLayout L = workspace_layout(plan);
-    if (bytes < L.total) return ZERO_ENOMEM;
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
-    char *base = static_cast<char *>(workspace);
-    if (!plan->segs.empty()) {
-        e = cudaMemcpyAsync(base + L.segs, plan->segs.data(), plan->segs.size() * sizeof(Seg), cudaMemcpyHostToDevice,
-                            reinterpret_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
-    }
-    plan->d_segs = reinterpret_cast<Seg *>(base + L.segs);
-    plan->d_partials = reinterpret_cast<double *>(base + L.partials);
-    plan->d_sqnorm = reinterpret_cast<double *>(base + L.scalars);
-    plan->d_coef = reinterpret_cast<float *>(base + L.scalars + 8);
-    plan->d_err = reinterpret_cast<int *>(base + L.scalars + 16);
-    plan->d_tickets = reinterpret_cast<unsigned long long *>(base + L.scalars + 24);
-    plan->d_skipped = reinterpret_cast<int *>(base + L.scalars + 40);
-    if (!plan->unit_table.empty()) {
-        e = cudaMemcpyAsync(base + L.units, plan->unit_table.data(), plan->unit_table.size() * sizeof(UnitDesc),
-                            cudaMemcpyHostToDevice, reinterpret_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
-    }
-    plan->d_units = reinterpret_cast<UnitDesc *>(base + L.units);
-    e = cudaMemsetAsync(base + L.scalars, 0, 256, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
-    plan->device = dev;
-    plan->attached = true;
-    return ZERO_OK;
-}
-
-extern "C" int zero_reduce_scatter(const zero_plan *plan, const void *const *grads, int32_t gdtype,
-                                   float *const *gshard, float coef, zero_stream_t stream) {
-    int rc = check_attached(plan);
-    if (rc != ZERO_OK) return rc;
-    if (!valid_dtype(gdtype)) return ZERO_EINVAL;
-    const int n = plan->n_ranks;
-    if ((rc = check_rank_ptrs(plan, grads, true)) != ZERO_OK) return rc;
-    if ((rc = check_rank_ptrs(plan, reinterpret_cast<const void *const *>(gshard), true)) != ZERO_OK) return rc;
-    KParams kp;
-    fill_common(plan, kp);
-    kp.coef = coef;
-    kp.write_g = 1;
-    for (int q = 0; q < n; ++q) {
-        kp.grads[q] = grads[q];
-        kp.gshard[q] = gshard[q];
-    }
-    return launch_pipe(MODE_REDUCE, gdtype, static_cast<int64_t>(plan->segs.size()), kp,
-                       reinterpret_cast<cudaStream_t>(stream));
-}
-
-// Pass 1 of a norm: per-segment partial sums (and optionally the gradient
-// shard), then the fixed-order total (and coefficient) on the device.
-static int launch_norm(const zero_plan *plan, const void *const *grads, int32_t gdtype, float *const *gshard,
-                       float max_norm, double *sqnorm_out, cudaStream_t st) {
-    KParams kp;
-    fill_common(plan, kp);
-    kp.want_partials = 1;
-    kp.write_g = gshard != nullptr;
-    for (int q = 0; q < plan->n_ranks; ++q) {
-        kp.grads[q] = grads[q];
-        if (gshard != nullptr) kp.gshard[q] = gshard[q];
-    }
-    const int64_t nseg = static_cast<int64_t>(plan->segs.size());
-    const int rc = launch_pipe(MODE_REDUCE, gdtype, nseg, kp, st);
-    if (rc != ZERO_OK) return rc;
-    k_finalize<<<1, kFinThreads, 0, st>>>(plan->d_partials, nseg, max_norm, plan->d_sqnorm, sqnorm_out, plan->d_coef,
-                                          plan->d_skipped);
-    return launch_status();
-}
-
-extern "C" int zero_grad_sqnorm(const zero_plan *plan, const void *const *grads, int32_t gdtype, double *sqnorm_dev,
-                                zero_stream_t stream) {
-    int rc = check_attached(plan);
-    if (rc != ZERO_OK) return rc;
-    if (!valid_dtype(gdtype) || sqnorm_dev == nullptr) return ZERO_EINVAL;
-    if ((reinterpret_cast<uintptr_t>(sqnorm_dev) & 7u) != 0) return ZERO_EALIGN;
-    if ((rc = check_rank_ptrs(plan, grads, true)) != ZERO_OK) return rc;
-    return launch_norm(plan, grads, gdtype, nullptr, 0.0f, sqnorm_dev, reinterpret_cast<cudaStream_t>(stream));
-}
-
-static int fill_state(const zero_plan *plan, KParams &kp, float *const *master, float *const *m, float *const *v,
-                      void *const *pshard, void *full, int32_t pdtype, const zero_hparams *hp) {
-    const int n = plan->n_ranks;
-    int rc;
-    if (!valid_dtype(pdtype) || hp == nullptr) return ZERO_EINVAL;
-    if ((rc = check_rank_ptrs(plan, reinterpret_cast<const void *const *>(master), true)) != ZERO_OK) return rc;
-    if ((rc = check_rank_ptrs(plan, reinterpret_cast<const void *const *>(m), true)) != ZERO_OK) return rc;
-    if ((rc = check_rank_ptrs(plan, reinterpret_cast<const void *const *>(v), true)) != ZERO_OK) return rc;
-    if ((rc = check_rank_ptrs(plan, pshard, false)) != ZERO_OK) return rc;
-    if ((rc = check_ptr(plan, full, false)) != ZERO_OK) return rc;
-    if ((rc = adam_consts(hp, &kp.c)) != ZERO_OK) return rc;
-    kp.pdtype = pdtype;
-    kp.full = full;
-    for (int q = 0; q < n; ++q) {
-        kp.master[q] = master[q];
-        kp.m[q] = m[q];
-        kp.v[q] = v[q];
-        kp.pshard[q] = pshard != nullptr ? pshard[q] : nullptr;
-    }
-    return ZERO_OK;
-}
-
-extern "C" int zero_adamw_shard_step(const zero_plan *plan, const float *const *gshard, float *const *master,
-                                     float *const *m, float *const *v, void *const *pshard, void *full, int32_t pdtype,
-                                     const zero_hparams *hp, zero_stream_t stream) {
-    int rc = check_attached(plan);
-    if (rc != ZERO_OK) return rc;
-    if ((rc = check_rank_ptrs(plan, reinterpret_cast<const void *const *>(gshard), true)) != ZERO_OK) return rc;
-    KParams kp;
-    fill_common(plan, kp);
-    if ((rc = fill_state(plan, kp, master, m, v, pshard, full, pdtype, hp)) != ZERO_OK) return rc;
-    for (int q = 0; q < plan->n_ranks; ++q) kp.gshard[q] = const_cast<float *>(gshard[q]);
-    return launch_pipe(MODE_SHARD, ZERO_F32, static_cast<int64_t>(plan->segs.size()), kp,
-                       reinterpret_cast<cudaStream_t>(stream));
-}
-
-extern "C" int zero_all_gather(const zero_plan *plan, const void *const *shard, void *full, int32_t pdtype, int32_t unit,
-                               zero_stream_t stream) {
-    int rc = check_attached(plan);
-    if (rc != ZERO_OK) return rc;
-    if (!valid_dtype(pdtype)) return ZERO_EINVAL;
-    if ((rc = check_rank_ptrs(plan, shard, true)) != ZERO_OK) return rc;
-    if ((rc = check_ptr(plan, full, true)) != ZERO_OK) return rc;
-    int64_t begin = 0, count = 0;
-    if ((rc = seg_range(plan, unit, begin, count)) != ZERO_OK) return rc;
-    KParams kp;
-    fill_common(plan, kp);
-    kp.seg_base = begin;
-    kp.pdtype = pdtype;
-    kp.full = full;
-    for (int q = 0; q < plan->n_ranks; ++q) kp.pshard[q] = const_cast<void *>(shard[q]);
-    if (count == 0) return ZERO_OK;
-    k_gather<<<static_cast<unsigned>(count), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(kp);
-    return launch_status();
-}
-
-extern "C" int zero_all_gather_unit(const zero_plan *plan, int32_t unit, const void *const *shard, void *dst_unit,
-                                    int32_t pdtype, zero_stream_t stream) {
-    int rc = check_attached(plan);
-    if (rc != ZERO_OK) return rc;
-    if (!valid_dtype(pdtype) || unit < 0 || unit >= plan->n_units) return ZERO_EINVAL;
-    int64_t begin = 0, count = 0;
-    if ((rc = seg_range(plan, unit, begin, count)) != ZERO_OK) return rc;
-    if (count == 0) return ZERO_OK;
-    if ((rc = check_rank_ptrs(plan, shard, true)) != ZERO_OK) return rc;
-    if (dst_unit == nullptr) return ZERO_EINVAL;
-    if (!aligned16(dst_unit)) return ZERO_EALIGN;
-    KParams kp;
-    fill_common(plan, kp);
-    kp.seg_base = begin;
-    kp.pdtype = pdtype;
-    kp.full = dst_unit;
-    kp.g_origin = plan->F[unit];
-    for (int q = 0; q < plan->n_ranks; ++q) kp.pshard[q] = const_cast<void *>(shard[q]);
-    k_gather<<<static_cast<unsigned>(count), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(kp);
-    return launch_status();
-}
-
-extern "C" int zero_all_gather_bf16(const zero_plan *plan, const uint16_t *const *shard16, uint16_t *full, int32_t unit,
-                                    zero_stream_t stream) {
-    return zero_all_gather(plan, reinterpret_cast<const void *const *>(shard16), full, ZERO_BF16, unit, stream);
-}
-
-extern "C" int zero_step(const zero_plan *plan, const void *const *grads, int32_t gdtype, float *const *master,
-                         float *const *m, float *const *v, void *full, void *const *pshard, int32_t pdtype,
-                         float *const *gshard_ws, const zero_hparams *hp, double *sqnorm_dev, int32_t unit,
-                         zero_stream_t stream) {
-    int rc = check_attached(plan);
-    if (rc != ZERO_OK) return rc;
-    if (!valid_dtype(gdtype) || hp == nullptr) return ZERO_EINVAL;
-    const int n = plan->n_ranks;
-    if ((rc = check_rank_ptrs(plan, grads, true)) != ZERO_OK) return rc;
-    const bool clip = hp->max_norm > 0.0f;
-    if (clip) {
-        if (unit != -1) return ZERO_EINVAL;  // the global norm needs every unit
-        if ((rc = check_rank_ptrs(plan, reinterpret_cast<const void *const *>(gshard_ws), true)) != ZERO_OK) return rc;
-        if (sqnorm_dev != nullptr && (reinterpret_cast<uintptr_t>(sqnorm_dev) & 7u) != 0) return ZERO_EALIGN;
-    }
-    int64_t begin = 0, count = 0;
-    if ((rc = seg_range(plan, unit, begin, count)) != ZERO_OK) return rc;
-    KParams kp;
-    fill_common(plan, kp);
-    if ((rc = fill_state(plan, kp, master, m, v, pshard, full, pdtype, hp)) != ZERO_OK) return rc;
-    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (!clip) {
-        for (int q = 0; q < n; ++q) kp.grads[q] = grads[q];
-        kp.seg_base = begin;
-        return launch_pipe(MODE_FUSED, gdtype, count, kp, st);
-    }
-    // clipped: norm pass (writes the averaged gradient shard), device
-    // coefficient, then the update from the shard scaled by that coefficient
-    if ((rc = launch_norm(plan, grads, gdtype, gshard_ws, hp->max_norm, sqnorm_dev, st)) != ZERO_OK) return rc;
-    for (int q = 0; q < n; ++q) kp.gshard[q] = gshard_ws[q];
-    kp.use_coef_dev = 1;
-    kp.coef_dev = plan->d_coef;
-    return launch_pipe(MODE_SHARD, ZERO_F32, count, kp, st);
-}
-
-// Unit-local variants: grads_unit[q] holds only unit u's S_u padded
-// gradient positions (element i = full position F_u + i).
-static int unit_common(const zero_plan *plan, int32_t unit, const void *const *grads_unit, int32_t gdtype,
-                       int64_t &begin, int64_t &count, KParams &kp) {
-    int rc = check_attached(plan);
-    if (rc != ZERO_OK) return rc;
-    if (!valid_dtype(gdtype) || unit < 0 || unit >= plan->n_units) return ZERO_EINVAL;
-    if ((rc = seg_range(plan, unit, begin, count)) != ZERO_OK) return rc;
-    fill_common(plan, kp);
-    kp.g_origin = plan->F[unit];
-    kp.g_len = plan->S[unit];
-    kp.seg_base = begin;
-    if (plan->S[unit] == 0) return ZERO_OK;
-    if (grads_unit == nullptr) return ZERO_EINVAL;
-    for (int q = 0; q < plan->n_ranks; ++q) {
-        if (grads_unit[q] == nullptr) return ZERO_EINVAL;
-        if (!aligned16(grads_unit[q])) return ZERO_EALIGN;
-        kp.grads[q] = grads_unit[q];
-    }
-    return ZERO_OK;
-}
-
-extern "C" int zero_step_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit, int32_t gdtype,
-                              float *const *master, float *const *m, float *const *v, void *full, void *const *pshard,
-                              int32_t pdtype, const zero_hparams *hp, zero_stream_t stream) {
-    if (hp == nullptr || hp->max_norm > 0.0f) return ZERO_EINVAL;  // a global clip needs every unit
-    int64_t begin = 0, count = 0;
-    KParams kp;
-    int rc = unit_common(plan, unit, grads_unit, gdtype, begin, count, kp);
-    if (rc != ZERO_OK || count == 0) return rc;
-    if ((rc = fill_state(plan, kp, master, m, v, pshard, full, pdtype, hp)) != ZERO_OK) return rc;
-    return launch_pipe(MODE_FUSED, gdtype, count, kp, reinterpret_cast<cudaStream_t>(stream));
-}
-
-extern "C" int zero_reduce_scatter_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit,
-                                        int32_t gdtype, float *const *gshard, float coef, zero_stream_t stream) {
-    int64_t begin = 0, count = 0;
-    KParams kp;
-    int rc = unit_common(plan, unit, grads_unit, gdtype, begin, count, kp);
-    if (rc != ZERO_OK || count == 0) return rc;
-    if ((rc = check_rank_ptrs(plan, reinterpret_cast<const void *const *>(gshard), true)) != ZERO_OK) return rc;
-    kp.coef = coef;
-    kp.write_g = 1;
-    for (int q = 0; q < plan->n_ranks; ++q) kp.gshard[q] = gshard[q];
-    return launch_pipe(MODE_REDUCE, gdtype, count, kp, reinterpret_cast<cudaStream_t>(stream));
-}
-
-extern "C" int zero_debug_drop_copy(int64_t tile) {
-    if (tile < -1) return ZERO_EINVAL;
-    g_drop_tile.store(tile);
-    return ZERO_OK;
-}
-
-extern "C" int zero_plan_check(const zero_plan *plan, zero_stream_t stream) {
-    int rc = check_attached(plan);
-    if (rc != ZERO_OK) return rc;
-    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    int32_t err = 0, skipped = 0;
-    cudaError_t e = cudaMemcpyAsync(&err, plan->d_err, sizeof(err), cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(&skipped, plan->d_skipped, sizeof(skipped), cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(plan->d_err, 0, sizeof(int32_t), st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(plan->d_skipped, 0, sizeof(int32_t), st);
-    if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
-    if (err != 0) return ZERO_ETIMEOUT;
-    if (skipped != 0) return ZERO_ENONFINITE;
-    return ZERO_OK;
-}
-
-extern "C" int zero_plan_device_errors(const zero_plan *plan, zero_stream_t stream, int32_t *errors) {
-    int rc = check_attached(plan);
-    if (rc != ZERO_OK) return rc;
-    if (errors == nullptr) return ZERO_EINVAL;
-    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    int32_t host = 0;
-    cudaError_t e = cudaMemcpyAsync(&host, plan->d_err, sizeof(host), cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(plan->d_err, 0, sizeof(int32_t), st);
-    if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
-    *errors = host;
-    return ZERO_OK;
-}
