@@ -887,8 +887,22 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(const double *partials
 }
 
 // ------------------------------------------------------------------ all-gather
-// full[F_u + r h_u + j] = shard[r][Hoff_u + j]: a copy per segment, 16-byte
-// vectors where the full position is aligned like the shard position.
+// full[F_u + r h_u + j] = shard[r][Hoff_u + j]: a copy per segment in 16-byte
+// vectors, whether or not the full position is aligned like the shard one.
+// Bytes [sb, sb + 16) of the 32-byte concatenation a:b (sb even, 0..14).
+__device__ __forceinline__ uint4 shift_pair(const uint4 &a, const uint4 &b, int sb) {
+    const uint32_t r = static_cast<uint32_t>(sb & 3) * 8u;  // 0 or 16 bits
+    uint32_t w0, w1, w2, w3, w4;
+    switch (sb >> 2) {
+        case 0: w0 = a.x; w1 = a.y; w2 = a.z; w3 = a.w; w4 = b.x; break;
+        case 1: w0 = a.y; w1 = a.z; w2 = a.w; w3 = b.x; w4 = b.y; break;
+        case 2: w0 = a.z; w1 = a.w; w2 = b.x; w3 = b.y; w4 = b.z; break;
+        default: w0 = a.w; w1 = b.x; w2 = b.y; w3 = b.z; w4 = b.w; break;
+    }
+    return make_uint4(__funnelshift_r(w0, w1, r), __funnelshift_r(w1, w2, r), __funnelshift_r(w2, w3, r),
+                      __funnelshift_r(w3, w4, r));
+}
+
 __global__ void __launch_bounds__(kThreads) k_gather(const KParams p) {
     const Seg sg = p.segs[p.seg_base + blockIdx.x];
     const SegSplit sp = split_segment(sg, p.g_origin);
@@ -897,14 +911,12 @@ __global__ void __launch_bounds__(kThreads) k_gather(const KParams p) {
     // destination element 0 is full position g_origin (0, or F_u for a unit-sized destination);
     // sp.gvec is the alignment relative to that origin
     char *dst = static_cast<char *>(p.full) + (sg.g_off - p.g_origin) * esz;
-    int i = threadIdx.x;
+    int head, tail0;  // elements [0, head) and [tail0, len) are copied one by one below
     if (sp.gvec) {
-        // aligned like the shard: whole 16-byte vectors, four groups per thread in flight
-        // (one group = 8 elements = 1 vector for bf16, 2 for fp32)
-        const int vpg = esz / 2;  // vectors per group
+        // aligned like the shard: whole 16-byte vectors, four in flight per thread
         const uint4 *s4 = reinterpret_cast<const uint4 *>(src + sp.k0 * esz);
         uint4 *d4 = reinterpret_cast<uint4 *>(dst + sp.k0 * esz);
-        const int nv = sp.ngroups * vpg;
+        const int nv = sp.ngroups * (esz / 2);  // a group is 8 elements: 1 vector (bf16) or 2 (fp32)
         int v = threadIdx.x;
         for (; v + 3 * kThreads < nv; v += 4 * kThreads) {
             const uint4 x0 = __ldcs(s4 + v), x1 = __ldcs(s4 + v + kThreads);
@@ -915,30 +927,36 @@ __global__ void __launch_bounds__(kThreads) k_gather(const KParams p) {
             __stcs(d4 + v + 3 * kThreads, x3);
         }
         for (; v < nv; v += kThreads) __stcs(d4 + v, __ldcs(s4 + v));
-        i = sp.ngroups;  // no groups left for the loop below
-    }
-    for (; i < sp.ngroups; i += kThreads) {  // destination not aligned like the shard: element stores
-        const int k = sp.k0 + 8 * i;
-        if (esz == 2) {
-            const uint4 x = __ldcs(reinterpret_cast<const uint4 *>(src + k * 2));
-            unsigned short *d = reinterpret_cast<unsigned short *>(dst) + k;
-            const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                d[2 * e] = static_cast<unsigned short>(w4[e] & 0xFFFFu);
-                d[2 * e + 1] = static_cast<unsigned short>(w4[e] >> 16);
-            }
-        } else {
-            float x[8];
-            load8(reinterpret_cast<const float *>(src) + k, x);
-            float *d = reinterpret_cast<float *>(dst) + k;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) d[e] = x[e];
+        head = sp.k0;
+        tail0 = sp.tail0;
+    } else {
+        // the destination is aligned differently from the shard: every aligned 16-byte
+        // destination vector is assembled from the two aligned source vectors it overlaps
+        // (both hold bytes of the segment, so no read leaves the aligned blocks it covers)
+        const int lenb = sg.len * esz;
+        const int e0b = static_cast<int>((16u - (reinterpret_cast<uintptr_t>(dst) & 15u)) & 15u);
+        const int nv = lenb > e0b ? (lenb - e0b) >> 4 : 0;
+        const uintptr_t sa = reinterpret_cast<uintptr_t>(src) + static_cast<uintptr_t>(e0b);
+        const int sb = static_cast<int>(sa & 15u);
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(sa - static_cast<uintptr_t>(sb));
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst + e0b);
+        int v = threadIdx.x;
+        for (; v + kThreads < nv; v += 2 * kThreads) {
+            const uint4 a0 = __ldcs(s4 + v), b0 = sb ? __ldcs(s4 + v + 1) : a0;
+            const uint4 a1 = __ldcs(s4 + v + kThreads), b1 = sb ? __ldcs(s4 + v + kThreads + 1) : a1;
+            __stcs(d4 + v, shift_pair(a0, b0, sb));
+            __stcs(d4 + v + kThreads, shift_pair(a1, b1, sb));
         }
+        for (; v < nv; v += kThreads) {
+            const uint4 a = __ldcs(s4 + v), b = sb ? __ldcs(s4 + v + 1) : a;
+            __stcs(d4 + v, shift_pair(a, b, sb));
+        }
+        head = nv > 0 ? e0b / esz : sg.len;
+        tail0 = nv > 0 ? (e0b + 16 * nv) / esz : sg.len;
     }
-    const int nedge = sp.k0 + (sg.len - sp.tail0);
+    const int nedge = head + (sg.len - tail0);
     for (int t = threadIdx.x; t < nedge; t += kThreads) {
-        const int k = t < sp.k0 ? t : sp.tail0 + (t - sp.k0);
+        const int k = t < head ? t : tail0 + (t - head);
         if (esz == 2) reinterpret_cast<unsigned short *>(dst)[k] = reinterpret_cast<const unsigned short *>(src)[k];
         else reinterpret_cast<float *>(dst)[k] = reinterpret_cast<const float *>(src)[k];
     }

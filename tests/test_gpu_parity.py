@@ -279,6 +279,37 @@ def test_all_gather_per_unit_and_fp32():
             assert np.array_equal(full.cpu().numpy()[c.map], ref)
 
 
+@pytest.mark.parametrize("N,pd", [(16, W.BF16), (16, W.F32), (3, W.BF16), (5, W.F32)])
+def test_all_gather_misaligned_slices_integer_exact(N, pd):
+    """Fine-wrap-shaped units: most slices land in the full buffer at positions
+    aligned differently from their shard positions (the shifted-vector path).
+    The gather of all units, per-unit gathers, and per-unit gathers into
+    unit-sized buffers all place every shard element at its full position."""
+    sizes = W.finewrap_units(n_units=200, lo_log2=0, hi_log2=15, seed=7)
+    c = SmallCase(sizes, N, W.BF16, pd, seed=N)
+    segs = Z.zero_plan_segments(c.plan.handle)
+    assert sum(1 for sg in segs if (sg[0] - sg[1]) % 8) > len(segs) // 2
+    g = torch.Generator().manual_seed(N)
+    src = aligned_copy(torch.randn(N, c.plan.H, generator=g).to(c.pshard.dtype), c.device)
+    want = np.zeros(c.plan.P_pad, dtype=np.uint32 if pd == W.F32 else np.uint16)
+    want[c.map.ravel()] = host_bits(src).ravel()
+    full = torch.zeros_like(c.full)
+    Z.zero_all_gather(c.plan, src, full)
+    assert np.array_equal(host_bits(full), want)
+    full.zero_()
+    for u in range(len(sizes)):
+        Z.zero_all_gather(c.plan, src, full, unit=u)
+    assert np.array_equal(host_bits(full), want)
+    for u in range(len(sizes)):
+        F, S = c.plan.F[u], c.plan.S[u]
+        if S == 0:
+            continue
+        buf = torch.zeros(S + 8, dtype=c.full.dtype, device=c.device)
+        Z.zero_all_gather_unit(c.plan, u, src, buf[:S])
+        assert np.array_equal(host_bits(buf[:S]), want[F:F + S]), u
+        assert not host_bits(buf[S:]).any()  # nothing written past the unit
+
+
 def test_grad_sqnorm_close_to_exact_and_deterministic():
     sizes = [70001, 3, 65537, 12345, 9]
     c = SmallCase(sizes, 8, W.BF16, W.BF16, seed=11, outlier_frac=1e-3, outlier_scale=100.0)
