@@ -437,6 +437,54 @@ def run_reshard(args, world, rank, local):
     return 0
 
 
+def run_gather(args, world, rank, local):
+    """The all-gather of every unit in one launch (k_gather): bf16 rank shards of the
+    workload's layout into the full parameter buffer, 4 bytes of HBM traffic per padded
+    element (2 read, 2 written).  Fine-wrap layouts exercise the misaligned path."""
+    import fsdp_sharded_optimizer_step_gb300 as Z
+    from fsdp_sharded_optimizer_step_gb300 import build as zbuild
+    from fsdp_sharded_optimizer_step_gb300 import workloads as W
+    zbuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = W.CONFIGS[args.config]
+    sizes = cfg["units"]()
+    N = cfg["N"]
+    plan = Z.ZeroPlan(sizes, N, dev)
+    pshard = Z.rank_buffers(N, plan.H, torch.bfloat16, dev)
+    pshard.normal_()
+    full = torch.empty(plan.P_pad, dtype=torch.bfloat16, device=dev)
+    segs = Z.zero_plan_segments(plan.handle)
+    misaligned = sum(1 for sg in segs if (sg[0] - sg[1]) % 8) / max(len(segs), 1)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        Z.zero_all_gather_bf16(plan, pshard, full)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        Z.zero_all_gather_bf16(plan, pshard, full)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    nbytes = 4 * plan.P_pad
+    gbs = nbytes / (ms / 1e3) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+    traffic = _summary_traffic(f"k_gather_{args.config}.md", kernel_source_hash())
+    if rank == 0:
+        print(json.dumps({"metric": "all-gather of every unit in one launch (GB/s of HBM traffic)", "value": world * gbs,
+                          "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                          "dtype": "bf16", "data": "synthetic",
+                          "config": {"workload": f"{args.config}: {cfg['desc']}", "bytes_per_step": nbytes,
+                                     "segments": len(segs), "misaligned_segment_fraction": misaligned},
+                          "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                                       "frac": gbs / peak, "traffic": traffic, "peak_kind": peak_kind},
+                          "gpu_launches": args.steps}), flush=True)
+    return 0
+
+
 def _time_ms(fn, stream, reps):
     fn()
     torch.cuda.synchronize()
@@ -542,8 +590,9 @@ def main():
                          "region (removes host launch overhead; the step counter t is the one captured)")
     ap.add_argument("--ref-sample", type=int, default=1 << 22)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--op", default="step", choices=["step", "reshard", "zero3_gather", "zero2_buckets"],
+    ap.add_argument("--op", default="step", choices=["step", "reshard", "gather", "zero3_gather", "zero2_buckets"],
                     help="step: the sharded optimizer step (default); reshard: checkpoint resharding of the state; "
+                         "gather: the all-gather of every unit in one launch; "
                          "zero3_gather: per-unit gathers with/without prefetch beside a synthetic per-unit GEMM; "
                          "zero2_buckets: bucketed reduce-scatter + shard update against the fused step")
     ap.add_argument("--to-ranks", type=int, default=0, help="reshard target rank count (default 2N)")
@@ -555,6 +604,8 @@ def main():
         return run_reference(args, world, rank)
     if args.op == "reshard":
         return run_reshard(args, world, rank, local)
+    if args.op == "gather":
+        return run_gather(args, world, rank, local)
     if args.op in ("zero3_gather", "zero2_buckets"):
         return run_unit_flows(args, world, rank, local)
 
