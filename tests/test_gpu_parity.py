@@ -530,6 +530,15 @@ def test_bounded_wait_runs_out_and_is_reported():
     c.gpu_step(2)
     assert Z.zero_plan_check(c.plan) == B.ZERO_ETIMEOUT
     assert Z.zero_plan_check(c.plan) == B.ZERO_OK
+    # the aborted launches left the same plan usable: its segment schedule starts clean, and a
+    # step from whatever state they left is exact again (the fused step and the clipped one)
+    for t, max_norm in ((3, 0.0), (4, 1e-3)):
+        c.reload()
+        c.gpu_step(t, max_norm=max_norm)
+        assert c.oracle_step(t, max_norm=max_norm) == O.OK
+        c.assert_state_equal()
+        c.assert_full_equal()
+        assert Z.zero_plan_check(c.plan) == B.ZERO_OK
     d = SmallCase([70001, 3000], 8, W.BF16, W.BF16, seed=52)
     d.gpu_step(1)
     assert d.oracle_step(1) == O.OK
