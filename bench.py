@@ -330,12 +330,14 @@ def update_bytes_per_element(cfg):
 E2E_PINNED_BUDGET = 32e9
 
 
-def measure_e2e(args, world, dev, stream, grads, full, step, N, P, gdt, pdt, psi, plan=None, state=None, streamed=False):
+def measure_e2e(args, world, dev, stream, grads, full, step, N, P, gdt, pdt, psi, plan=None, state=None, streamed=False,
+                max_norm=0.0, gshard=None):
     """Same metric through the public API with host buffers: every step takes the
     N gradient buffers from pinned host memory and returns the gathered params to
     pinned host memory.  streamed: unit by unit (HostStreamedStep: copy-in of the
-    next unit, update of this one and copy-out of finished ones overlap);
-    otherwise all gradients are copied in, the step runs, the params are copied out."""
+    next unit, its update -- or, clipped, its norm pass -- and copy-out of finished
+    ones overlap); otherwise all gradients are copied in, the step runs, the params
+    are copied out."""
     e2e_steps = max(3, min(args.steps, 10))
     h_grads = torch.empty(N, P, dtype=gdt, pin_memory=True)
     for r in range(N):
@@ -350,7 +352,11 @@ def measure_e2e(args, world, dev, stream, grads, full, step, N, P, gdt, pdt, psi
         master, m, v = state
 
         def e2e_step(t):
-            streamer.step(h_grads, master, m, v, AdamW(t=t, **W.HP), full, host_full=h_full)
+            hp = AdamW(t=t, max_norm=max_norm, **W.HP)
+            if max_norm > 0:
+                streamer.step_clipped(h_grads, gshard, master, m, v, hp, full, host_full=h_full)
+            else:
+                streamer.step(h_grads, master, m, v, hp, full, host_full=h_full)
     else:
         def e2e_step(t):
             for r in range(N):
@@ -378,7 +384,8 @@ def measure_e2e(args, world, dev, stream, grads, full, step, N, P, gdt, pdt, psi
            # the fastest step reached (all copied bytes over its time)
            "median_ms": statistics.median(per_step), "min_ms": min(per_step), "max_ms": max(per_step),
            "link_GBs_at_min": (h2d + d2h) / (min(per_step) / 1e3) / 1e9,
-           "mode": "streamed per unit: copy-in, update and copy-out overlapped" if streamed
+           "mode": ("streamed per unit: copy-in, norm pass, then update and copy-out overlapped" if max_norm > 0
+                    else "streamed per unit: copy-in, update and copy-out overlapped") if streamed
            else "copy all gradients in, step, copy params out"}
     del h_grads, h_full
     return e2e
@@ -707,7 +714,8 @@ def main():
     pinned_bytes = N * P * grads.element_size() + P * full.element_size()
     if pinned_bytes <= E2E_PINNED_BUDGET:
         e2e = measure_e2e(args, world, dev, stream, grads, full, step, N, P, gdt, pdt, psi, plan=plan,
-                          state=(master, m, v), streamed=not (clip or z3 or args.per_unit))
+                          state=(master, m, v), streamed=not (z3 or args.per_unit),
+                          max_norm=cfg.get("max_norm", 0.0), gshard=gshard)
     else:
         e2e = {"value": None, "unit": UNIT, "skipped": f"{pinned_bytes / 1e9:.0f} GB of pinned host buffers "
                                                        f"exceeds the {E2E_PINNED_BUDGET / 1e9:.0f} GB budget"}

@@ -87,6 +87,9 @@ def lib():
             "zero_reshard": (C.c_int, [p, p, pp, pp, i32, p]),
             "zero_all_gather_unit": (C.c_int, [p, i32, pp, p, i32, p]),
             "zero_reduce_scatter_unit": (C.c_int, [p, i32, pp, i32, pp, f32, p]),
+            "zero_clip_reduce_unit": (C.c_int, [p, i32, pp, i32, pp, p]),
+            "zero_clip_finalize": (C.c_int, [p, f32, p, p]),
+            "zero_adamw_shard_step_clipped": (C.c_int, [p, pp, pp, pp, pp, pp, p, i32, p, i32, p]),
             "zero_plan_device_errors": (C.c_int, [p, p, p]),
             "zero_plan_check": (C.c_int, [p, p]),
             "zero_debug_drop_copy": (C.c_int, [i64]),
@@ -388,6 +391,38 @@ def zero_reduce_scatter_unit(plan, unit, grads_unit, gshard, coef=1.0, stream=No
     gs, _ = _rows(plan, gshard, plan.H, "gshard", _F)
     _check(lib().zero_reduce_scatter_unit(plan.handle, int(unit), g, gd, gs, float(coef), _stream(stream, plan.device)),
            "zero_reduce_scatter_unit")
+
+
+def zero_clip_reduce_unit(plan, unit, grads_unit, gshard, stream=None):
+    """Clipped step, pass 1 for one unit (see include/zero.h): averaged gradient shard + sums of squares."""
+    g, gd = _rows(plan, grads_unit, plan.S[unit], "grads_unit", _G)
+    gs, _ = _rows(plan, gshard, plan.H, "gshard", _F)
+    _check(lib().zero_clip_reduce_unit(plan.handle, int(unit), g, gd, gs, _stream(stream, plan.device)),
+           "zero_clip_reduce_unit")
+
+
+def zero_clip_finalize(plan, max_norm, sqnorm_out=None, stream=None):
+    """Clipped step, pass 2: S over every unit and the clip coefficient, on the device."""
+    sq = None
+    if sqnorm_out is not None:
+        if sqnorm_out.device != plan.device or sqnorm_out.dtype != torch.float64 or sqnorm_out.numel() < 1:
+            raise ValueError("sqnorm_out: need a float64 tensor on the plan's device")
+        sq = C.c_void_p(sqnorm_out.data_ptr())
+    _check(lib().zero_clip_finalize(plan.handle, float(max_norm), sq, _stream(stream, plan.device)),
+           "zero_clip_finalize")
+
+
+def zero_adamw_shard_step_clipped(plan, gshard, master, m, v, hp: AdamW, pshard=None, full=None, unit=-1,
+                                  stream=None):
+    """Clipped step, pass 3: the shard update scaled by the device coefficient (all units or one)."""
+    gs, _ = _rows(plan, gshard, plan.H, "gshard", _F)
+    W, _ = _rows(plan, master, plan.H, "master", _F)
+    M, _ = _rows(plan, m, plan.H, "m", _F)
+    V, _ = _rows(plan, v, plan.H, "v", _F)
+    fp, ps, pdt = _outputs(plan, full, pshard)
+    c = hp.c()
+    _check(lib().zero_adamw_shard_step_clipped(plan.handle, gs, W, M, V, ps, fp, pdt, C.byref(c), int(unit),
+                                               _stream(stream, plan.device)), "zero_adamw_shard_step_clipped")
 
 
 def zero_reshard(plan_from, plan_to, src, dst, stream=None):

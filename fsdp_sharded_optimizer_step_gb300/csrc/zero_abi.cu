@@ -327,6 +327,47 @@ extern "C" int zero_reduce_scatter_unit(const zero_plan *plan, int32_t unit, con
     return launch_pipe(MODE_REDUCE, gdtype, count, kp, reinterpret_cast<cudaStream_t>(stream));
 }
 
+extern "C" int zero_clip_reduce_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit,
+                                     int32_t gdtype, float *const *gshard, zero_stream_t stream) {
+    int64_t begin = 0, count = 0;
+    KParams kp;
+    int rc = unit_common(plan, unit, grads_unit, gdtype, begin, count, kp);
+    if (rc != ZERO_OK || count == 0) return rc;
+    if ((rc = check_rank_ptrs(plan, reinterpret_cast<const void *const *>(gshard), true)) != ZERO_OK) return rc;
+    kp.write_g = 1;
+    kp.want_partials = 1;  // this unit's segments' sums of squares, at their table positions
+    for (int q = 0; q < plan->n_ranks; ++q) kp.gshard[q] = gshard[q];
+    return launch_pipe(MODE_REDUCE, gdtype, count, kp, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int zero_clip_finalize(const zero_plan *plan, float max_norm, double *sqnorm_dev, zero_stream_t stream) {
+    int rc = check_attached(plan);
+    if (rc != ZERO_OK) return rc;
+    if (!(max_norm > 0.0f)) return ZERO_EINVAL;
+    if (sqnorm_dev != nullptr && (reinterpret_cast<uintptr_t>(sqnorm_dev) & 7u) != 0) return ZERO_EALIGN;
+    return launch_finalize(plan->d_partials, static_cast<int64_t>(plan->segs.size()), max_norm, plan->d_sqnorm,
+                           sqnorm_dev, plan->d_coef, plan->d_skipped, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int zero_adamw_shard_step_clipped(const zero_plan *plan, const float *const *gshard, float *const *master,
+                                             float *const *m, float *const *v, void *const *pshard, void *full,
+                                             int32_t pdtype, const zero_hparams *hp, int32_t unit,
+                                             zero_stream_t stream) {
+    int rc = check_attached(plan);
+    if (rc != ZERO_OK) return rc;
+    if ((rc = check_rank_ptrs(plan, reinterpret_cast<const void *const *>(gshard), true)) != ZERO_OK) return rc;
+    int64_t begin = 0, count = 0;
+    if ((rc = seg_range(plan, unit, begin, count)) != ZERO_OK) return rc;
+    KParams kp;
+    fill_common(plan, kp);
+    if ((rc = fill_state(plan, kp, master, m, v, pshard, full, pdtype, hp)) != ZERO_OK) return rc;
+    for (int q = 0; q < plan->n_ranks; ++q) kp.gshard[q] = const_cast<float *>(gshard[q]);
+    kp.seg_base = begin;
+    kp.use_coef_dev = 1;  // the coefficient zero_clip_finalize left on the device (NaN: skip)
+    kp.coef_dev = plan->d_coef;
+    return launch_pipe(MODE_SHARD, ZERO_F32, count, kp, reinterpret_cast<cudaStream_t>(stream));
+}
+
 extern "C" int zero_debug_drop_copy(int64_t tile) {
     if (tile < -1) return ZERO_EINVAL;
     arm_drop_tile(tile);

@@ -253,6 +253,33 @@ int zero_step_unit(const zero_plan *plan, int32_t unit, const void *const *grads
 int zero_reduce_scatter_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit, int32_t gdtype,
                              float *const *gshard, float coef, zero_stream_t stream);
 
+/* The clipped step with the gradients streamed in unit by unit (the norm needs
+ * every unit before any update, "ZeRO and FSDP sharding", Implementation
+ * notes; a norm is a decomposable sum of squares, "ZeRO: Three Ledgers, Zero
+ * Redundancy", section 2).  Three calls, in this order on one stream:
+ *
+ * 1. zero_clip_reduce_unit for every unit with S_u > 0, in any order, each
+ *    from unit-local gradient buffers (as zero_step_unit): writes the unit's
+ *    averaged fp32 gradient into gshard[r][Hoff_u + j] and the sums of squares
+ *    of the unit's launch-table segments into the plan's workspace.
+ * 2. zero_clip_finalize: adds every segment's sum in table order (the same
+ *    fixed order as zero_step) into S (*sqnorm_dev, DEVICE, 8-byte aligned,
+ *    optional) and the clip coefficient min(1, max_norm / (sqrt(S) + 1e-6)),
+ *    both kept on the device; S not finite skips the update of step 3 (and
+ *    zero_plan_check then reports ZERO_ENONFINITE).
+ * 3. zero_adamw_shard_step_clipped for all units (unit = -1) or unit by unit:
+ *    zero_adamw_shard_step from gshard scaled by that coefficient.
+ *
+ * master/m/v, params and S equal those of a clipped zero_step bit for bit.
+ * Errors: as zero_step_unit / zero_adamw_shard_step; zero_clip_finalize
+ * returns ZERO_EINVAL for max_norm <= 0. */
+int zero_clip_reduce_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit, int32_t gdtype,
+                          float *const *gshard, zero_stream_t stream);
+int zero_clip_finalize(const zero_plan *plan, float max_norm, double *sqnorm_dev, zero_stream_t stream);
+int zero_adamw_shard_step_clipped(const zero_plan *plan, const float *const *gshard, float *const *master,
+                                  float *const *m, float *const *v, void *const *pshard, void *full, int32_t pdtype,
+                                  const zero_hparams *hp, int32_t unit, zero_stream_t stream);
+
 /* ---------------------------------------------------------------- checkpoint resharding */
 
 /* Reshard a per-rank array between two layouts of the same units ("ZeRO and

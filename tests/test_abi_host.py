@@ -148,6 +148,11 @@ def test_argument_errors_are_reported_on_the_host(zlib):
     for s in (-5, -6):  # the statuses zero_plan_check reports have their own text
         assert L.zero_status_string(s) != L.zero_status_string(-99)
     assert L.zero_plan_check(h, None) == B.ZERO_ENOTATTACHED
+    assert L.zero_clip_reduce_unit(h, 0, ptrs, B.ZERO_BF16, ptrs, None) == B.ZERO_ENOTATTACHED
+    assert L.zero_clip_finalize(h, C.c_float(1.0), None, None) == B.ZERO_ENOTATTACHED
+    assert L.zero_adamw_shard_step_clipped(h, ptrs, ptrs, ptrs, ptrs, None, None, B.ZERO_BF16, C.byref(hp), -1,
+                                           None) == B.ZERO_ENOTATTACHED
+    assert L.zero_clip_finalize(None, C.c_float(1.0), None, None) == B.ZERO_EINVAL
     assert L.zero_plan_check(None, None) == B.ZERO_EINVAL
     L.zero_plan_destroy(h)
     L.zero_plan_destroy(None)

@@ -231,6 +231,46 @@ def test_host_streamed_step_equals_device_step():
     assert np.array_equal(host_bits(host_full), host_bits(a.full))
 
 
+@pytest.mark.parametrize("max_norm", [1e-3, 1e6])
+def test_host_streamed_clipped_step_equals_device_clipped_step(max_norm):
+    """The clipped step with the gradients streamed in from pinned host memory
+    (per-unit norm passes, device total, per-unit shard updates with the params
+    copied back) gives the bits of the clipped zero_step, S included, and the
+    oracle's step; a coefficient below 1 and one that is exactly 1."""
+    from fsdp_sharded_optimizer_step_gb300 import binding as B
+    from fsdp_sharded_optimizer_step_gb300.streaming import HostStreamedStep
+    sizes = [70001, 3, 65537, 12345, 0, 9, 1 << 20]
+    a = SmallCase(sizes, 8, W.BF16, W.BF16, seed=23, grad_sigma=1e-2, outlier_frac=1e-3, outlier_scale=100.0)
+    b = SmallCase(sizes, 8, W.BF16, W.BF16, seed=23, grad_sigma=1e-2, outlier_frac=1e-3, outlier_scale=100.0)
+    host_grads = torch.empty(8, b.plan.P_pad, dtype=torch.bfloat16, pin_memory=True)
+    host_grads.copy_(b.grads.cpu())
+    host_full = torch.zeros(b.plan.P_pad, dtype=torch.bfloat16, pin_memory=True)
+    streamer = HostStreamedStep(b.plan, torch.bfloat16)
+    for t in (1, 2):
+        a.gpu_step(t, max_norm=max_norm, pshard=False)
+        hp, _ = hp_for(t, max_norm)
+        streamer.step_clipped(host_grads, b.gshard, b.master, b.m, b.v, hp, b.full, host_full=host_full,
+                              sqnorm_out=b.sq)
+        torch.cuda.synchronize()
+        assert b.sq.item() == a.sq.item()  # same segments, same fixed order
+        assert b.oracle_step(t, max_norm=max_norm) == O.OK
+        b.assert_state_equal()
+        b.assert_full_equal()
+    for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v), (a.full, b.full), (a.gshard, b.gshard)):
+        assert torch.equal(host_bits_t(x), host_bits_t(y))
+    assert np.array_equal(host_bits(host_full), host_bits(a.full))
+    assert Z.zero_plan_check(b.plan) == B.ZERO_OK
+    # a non-finite norm: the streamed step leaves the state alone and says so
+    host_grads[3, 17] = float("inf")
+    before = [x.clone() for x in (b.master, b.m, b.v, b.full)]
+    hp, _ = hp_for(3, max_norm)
+    streamer.step_clipped(host_grads, b.gshard, b.master, b.m, b.v, hp, b.full, sqnorm_out=b.sq)
+    assert Z.zero_plan_check(b.plan) == B.ZERO_ENONFINITE
+    assert math.isinf(b.sq.item())
+    for x, y in zip(before, (b.master, b.m, b.v, b.full)):
+        assert torch.equal(host_bits_t(x), host_bits_t(y))
+
+
 # ------------------------------------------------------------------ unfused parts
 def test_parts_compose_to_the_fused_step():
     """reduce-scatter -> AdamW on the shard -> all-gather == the fused step, bit for bit;
