@@ -59,13 +59,28 @@ def save(path, plan, arrays: dict, step: int):
 
 
 def load(path, plan, stream=None):
-    """Returns ({name: [N', H'] device tensors in plan's layout}, step)."""
+    """Returns ({name: [N', H'] device tensors in plan's layout}, step).
+
+    stream: the CUDA stream the copies and the reshard run on (default: the
+    current stream).  The whole load runs with that stream current, so the
+    staging buffers are allocated, filled, read and released on the one stream
+    that uses them (the caching allocator cannot hand a buffer the reshard is
+    still reading to the next array's copies)."""
     with open(os.path.join(path, "layout.json")) as f:
         layout = json.load(f)
     if [int(s) for s in layout["unit_sizes"]] != plan.unit_sizes:
         raise ValueError("checkpoint units differ from the plan's")
-    n_old, H_old = int(layout["n_ranks"]), int(layout["H"])
     dev = plan.device
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev), torch.cuda.stream(stream):
+        out = _load_arrays(path, layout, plan, dev, stream)
+    stream.synchronize()
+    return out, int(layout["step"])
+
+
+def _load_arrays(path, layout, plan, dev, stream):
+    n_old, H_old = int(layout["n_ranks"]), int(layout["H"])
     old = B.ZeroPlan(layout["unit_sizes"], n_old, dev, stream=stream) if n_old != plan.n_ranks else None
     out = {}
     offset = 0  # bytes into every rank file
@@ -85,8 +100,4 @@ def load(path, plan, stream=None):
             B.zero_reshard(old, plan, src, dst, stream=stream)
             out[spec["name"]] = dst
         offset += H_old * np.dtype(ndt).itemsize
-    if stream is not None:
-        stream.synchronize()
-    else:
-        torch.cuda.synchronize(dev)
-    return out, int(layout["step"])
+    return out

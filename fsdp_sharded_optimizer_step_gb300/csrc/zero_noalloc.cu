@@ -87,25 +87,43 @@ __global__ void __launch_bounds__(1024) k_sqnorm_total(const double *partials, i
     if (threadIdx.x == 0) *out = t;
 }
 
-// Device address of the scratch array on the current device, looked up once
-// per device (cudaGetSymbolAddress) and cached.
+// Set-up, once per device, with that device current: load this file's code
+// onto the device and look up the scratch array's device address.  Under
+// CUDA's lazy module loading the code would otherwise be loaded at the first
+// launch, and loading takes device memory: a first launch made after memory
+// ran out could fail.  cudaGetSymbolAddress loads the module that holds the
+// array, cudaFuncGetAttributes loads each kernel.  The address is cached per
+// device ordinal, so it assumes the device's context lives as long as the
+// process (a cudaDeviceReset would leave a stale address behind).
 std::mutex g_lock;
 std::unordered_map<int, double *> g_scratch_by_device;
 
-int scratch_on_current_device(double **out) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) { zero::set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
+int scratch_on_current_device(int dev, double **out) {
     std::lock_guard<std::mutex> guard(g_lock);
     auto it = g_scratch_by_device.find(dev);
     if (it == g_scratch_by_device.end()) {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_sqnorm_scratch);
+        cudaError_t e = cudaGetSymbolAddress(&p, g_sqnorm_scratch);
+        cudaFuncAttributes attr;
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&attr, k_sqnorm_chunks);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&attr, k_sqnorm_total);
         if (e != cudaSuccess || p == nullptr) { zero::set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
         it = g_scratch_by_device.emplace(dev, static_cast<double *>(p)).first;
     }
     *out = it->second;
     return ZERO_OK;
+}
+
+// Whether ptr is device (or managed) memory of device `dev`.  A host pointer,
+// or memory of another GPU, is refused before anything is launched.
+bool on_device(const void *ptr, int dev) {
+    cudaPointerAttributes a;
+    const cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // reset the runtime's last-error state
+        return false;
+    }
+    return (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) && a.device == dev;
 }
 
 }  // namespace
@@ -124,9 +142,16 @@ extern "C" int zero_grad_sqnorm_noalloc(const void *const *grads, int32_t n_rank
         if ((reinterpret_cast<uintptr_t>(grads[q]) & (esize - 1)) != 0) return ZERO_EALIGN;
         a.grads[q] = grads[q];
     }
+    int dev = -1;
+    const cudaError_t de = cudaGetDevice(&dev);
+    if (de != cudaSuccess) { zero::set_last_cuda_error(static_cast<int>(de)); return ZERO_ECUDA; }
     double *scratch = nullptr;
-    int rc = scratch_on_current_device(&scratch);
+    int rc = scratch_on_current_device(dev, &scratch);
     if (rc != ZERO_OK) return rc;
+    if (!on_device(sqnorm_dev, dev)) return ZERO_EINVAL;
+    if (n > 0)
+        for (int q = 0; q < n_ranks; ++q)
+            if (!on_device(grads[q], dev)) return ZERO_EINVAL;
     a.n_ranks = n_ranks;
     a.gdtype = gdtype;
     a.pow2 = (n_ranks & (n_ranks - 1)) == 0;

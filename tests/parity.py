@@ -59,11 +59,51 @@ def mismatch(got, want):
     return bad
 
 
-def aligned_copy(src: torch.Tensor, device):
-    """Copy a [N, L] tensor into rank buffers whose rows are 16-byte aligned."""
-    out = Z.rank_buffers(src.shape[0], src.shape[1], src.dtype, device)
+def aligned_copy(src: torch.Tensor, device, guards=None):
+    """Copy a [N, L] tensor into rank buffers whose rows are 16-byte aligned
+    (guarded ones when a guard list is given)."""
+    if guards is None:
+        out = Z.rank_buffers(src.shape[0], src.shape[1], src.dtype, device)
+    else:
+        out = guarded_buffers(guards, src.shape[1], src.dtype, device, rows=src.shape[0])
     out.copy_(src)
     return out
+
+
+# Guard bands: every device buffer of a small case sits inside a larger allocation
+# whose other bytes hold a canary pattern; a kernel that writes outside the
+# elements it was given (before a row, past its end, into the row padding)
+# changes a canary, which check_guards finds after the step.
+CANARY = 0xA5
+GUARD_BYTES = 64
+
+
+def guarded_buffers(guards: list, length, dtype, device, rows=None, zero=False):
+    """A [rows, length] view (or a 1-D view of `length` when rows is None) whose rows
+    start 16-byte aligned, inside an allocation with GUARD_BYTES of canary before
+    and after every row; (allocation, canary mask) is appended to `guards`."""
+    esz = torch.empty((), dtype=dtype).element_size()
+    g = GUARD_BYTES // esz
+    per16 = 16 // esz
+    stride = max((length + per16 - 1) // per16 * per16, 1)
+    n = 1 if rows is None else rows
+    backing = torch.empty(n, g + stride + g, dtype=dtype, device=device)
+    backing.view(torch.uint8).fill_(CANARY)
+    mask = torch.ones(n, (g + stride + g) * esz, dtype=torch.bool, device=device)
+    mask[:, g * esz:(g + length) * esz] = False
+    guards.append((backing, mask))
+    view = backing[:, g:g + length]
+    if zero:
+        view.zero_()
+    return view[0] if rows is None else view
+
+
+def check_guards(guards: list):
+    """Every canary byte of every guarded allocation is intact."""
+    for k, (backing, mask) in enumerate(guards):
+        u8 = backing.view(torch.uint8)
+        bad = int((u8[mask] != CANARY).sum().item())
+        assert bad == 0, f"guarded buffer {k}: {bad} canary bytes overwritten"
 
 
 def hp_for(t, max_norm=0.0, **over):
@@ -83,17 +123,19 @@ class SmallCase:
         self.o = O.Plan(self.sizes, N)
         assert self.plan.P_pad == self.o.P_pad and self.plan.H == self.o.H
         P, H = self.plan.P_pad, self.plan.H
+        self.guards = []  # every device buffer below sits between canary bands
         self.grads = aligned_copy(W.make_grads(N, P, gdtype, sigma=grad_sigma, device="cpu", seed=seed + 1,
-                                               outlier_frac=outlier_frac, outlier_scale=outlier_scale), self.device)
+                                               outlier_frac=outlier_frac, outlier_scale=outlier_scale), self.device,
+                                  self.guards)
         master, m, v = W.make_state(N, H, device="cpu", seed=seed + 1000)
         if state == "random":  # non-zero moments exercise every term of the update
             g = torch.Generator().manual_seed(seed + 7)
             m = torch.randn(N, H, generator=g) * 1e-3
             v = torch.rand(N, H, generator=g) * 1e-6
-        self.master, self.m, self.v = (aligned_copy(x, self.device) for x in (master, m, v))
-        self.full = torch.zeros(P, dtype=TDT[pdtype], device=self.device)
-        self.pshard = Z.rank_buffers(N, H, TDT[pdtype], self.device, zero=True)
-        self.gshard = Z.rank_buffers(N, H, torch.float32, self.device, zero=True)
+        self.master, self.m, self.v = (aligned_copy(x, self.device, self.guards) for x in (master, m, v))
+        self.full = guarded_buffers(self.guards, P, TDT[pdtype], self.device, zero=True)
+        self.pshard = guarded_buffers(self.guards, H, TDT[pdtype], self.device, rows=N, zero=True)
+        self.gshard = guarded_buffers(self.guards, H, torch.float32, self.device, rows=N, zero=True)
         self.sq = torch.zeros(1, dtype=torch.float64, device=self.device)
         # oracle state in the full (unsharded) layout
         self.map = self.o.shard_map()  # [N, H] -> full position
@@ -121,6 +163,10 @@ class SmallCase:
                     full=self.full if full else None, pshard=self.pshard if pshard else None,
                     gshard_ws=self.gshard if max_norm > 0 else None, sqnorm_out=self.sq if max_norm > 0 else None,
                     unit=unit)
+        self.check_guards()
+
+    def check_guards(self):
+        check_guards(self.guards)
 
     def oracle_step(self, t, max_norm=0.0, **over):
         _, ohp = hp_for(t, max_norm, **over)
@@ -133,6 +179,7 @@ class SmallCase:
 
     # -------------------------------------------------------------- comparisons
     def assert_state_equal(self):
+        self.check_guards()
         mp = self.map
         for name, gpu, ora in (("master", self.master, self.w_o), ("m", self.m, self.m_o), ("v", self.v, self.v_o)):
             got = host_bits(gpu)
@@ -141,6 +188,7 @@ class SmallCase:
             assert bad.size == 0, f"{name}: {bad.shape[0]} of {got.size} differ, first at rank/pos {bad[0]}"
 
     def assert_full_equal(self):
+        self.check_guards()
         got = host_bits(self.full)
         want = self.out_o if self.pdtype == W.BF16 else f32bits(self.out_o)
         bad = np.flatnonzero(mismatch(got, want))

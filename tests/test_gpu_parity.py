@@ -142,6 +142,10 @@ def test_per_unit_launches_equal_one_multi_unit_launch():
         b.gpu_step(1, unit=u)
     for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v), (a.full, b.full), (a.pshard, b.pshard)):
         assert torch.equal(host_bits_t(x), host_bits_t(y))
+    assert b.oracle_step(1) == O.OK  # the per-unit side against the oracle too
+    b.assert_state_equal()
+    b.assert_full_equal()
+    b.assert_pshard_equal()
 
 
 def test_per_unit_steps_replay_from_a_cuda_graph():
@@ -195,18 +199,26 @@ def test_unit_local_step_equals_full_step(N, gd):
         Z.zero_step_unit(b.plan, u, _unit_rows(b, u), b.master, b.m, b.v, hp, full=b.full, pshard=b.pshard)
     for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v), (a.full, b.full), (a.pshard, b.pshard)):
         assert torch.equal(host_bits_t(x), host_bits_t(y))
-    assert a.oracle_step(1) == O.OK
-    a.assert_full_equal()
+    assert b.oracle_step(1) == O.OK
+    b.assert_state_equal()
+    b.assert_full_equal()
+    b.assert_pshard_equal()
 
 
 def test_unit_local_reduce_scatter_equals_full():
+    """zero_reduce_scatter_unit over every unit from unit-local buffers: the oracle's
+    averaged gradient times the coefficient (one binary32 multiply) at every shard
+    position, and the same bits as the all-units zero_reduce_scatter."""
     sizes = W.finewrap_units(n_units=40, lo_log2=0, hi_log2=16, seed=10)
     c = SmallCase(sizes, 8, W.BF16, W.BF16, seed=10)
-    Z.zero_reduce_scatter(c.plan, c.grads, c.gshard, coef=0.5)
+    coef = np.float32(0.3711)
+    for u in range(len(sizes)):
+        Z.zero_reduce_scatter_unit(c.plan, u, _unit_rows(c, u), c.gshard, coef=float(coef))
+    want = (O.avg_grad(c.g_o, O.BF16, c.pad) * coef).astype(np.float32)
+    assert np.array_equal(host_bits(c.gshard), f32bits(want)[c.map])
     ref = host_bits(c.gshard).copy()
     c.gshard.zero_()
-    for u in range(len(sizes)):
-        Z.zero_reduce_scatter_unit(c.plan, u, _unit_rows(c, u), c.gshard, coef=0.5)
+    Z.zero_reduce_scatter(c.plan, c.grads, c.gshard, coef=float(coef))
     assert np.array_equal(host_bits(c.gshard), ref)
 
 
@@ -225,7 +237,11 @@ def test_host_streamed_step_equals_device_step():
         a.gpu_step(t, pshard=False)
         hp, _ = hp_for(t)
         streamer.step(host_grads, b.master, b.m, b.v, hp, b.full, host_full=host_full)
-    torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        assert b.oracle_step(t) == O.OK  # the streamed side against the oracle, every step
+        b.assert_state_equal()
+        b.assert_full_equal()
+        assert np.array_equal(host_bits(host_full), b.out_o)
     for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v), (a.full, b.full)):
         assert torch.equal(host_bits_t(x), host_bits_t(y))
     assert np.array_equal(host_bits(host_full), host_bits(a.full))
@@ -288,8 +304,10 @@ def test_parts_compose_to_the_fused_step():
     for x, y in ((fused.master, parts.master), (fused.m, parts.m), (fused.v, parts.v), (fused.full, parts.full),
                  (fused.pshard, parts.pshard)):
         assert torch.equal(host_bits_t(x), host_bits_t(y))
-    assert fused.oracle_step(1) == O.OK
-    fused.assert_full_equal()
+    assert parts.oracle_step(1) == O.OK
+    parts.assert_state_equal()
+    parts.assert_pshard_equal()
+    parts.assert_full_equal()
 
 
 def test_reduce_scatter_with_coefficient():
@@ -506,13 +524,35 @@ def test_sharded_checkpoint_reshard_then_continue(tmp_path):
     c4.assert_full_equal()
 
 
+def test_checkpoint_load_on_a_side_stream(tmp_path):
+    """load() given a stream that is not the current one: seven arrays (fp32 and bf16)
+    resharded 8 -> 3 on that stream, back to back, each equal to the oracle's remap
+    (one array's staging buffers are not reused by the next array's copies while its
+    reshard still reads them)."""
+    from fsdp_sharded_optimizer_step_gb300 import checkpoint
+    sizes = W.finewrap_units(n_units=30, lo_log2=8, hi_log2=20, seed=5) + [1 << 20]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    p8, p3 = Z.ZeroPlan(sizes, 8, dev), Z.ZeroPlan(sizes, 3, dev)
+    g = torch.Generator().manual_seed(77)
+    arrays = {f"a{k}": aligned_copy(torch.randn(8, p8.H, generator=g), dev) for k in range(6)}
+    arrays["p16"] = aligned_copy(torch.randn(8, p8.H, generator=g).to(torch.bfloat16), dev)
+    checkpoint.save(str(tmp_path), p8, arrays, step=5)
+    side = torch.cuda.Stream()
+    state, step = checkpoint.load(str(tmp_path), p3, stream=side)
+    assert step == 5 and list(state) == list(arrays)
+    for name, a in arrays.items():
+        assert np.array_equal(host_bits(state[name]), O.reshard(sizes, 8, 3, host_bits(a))), name
+
+
 # ------------------------------------------------------------------ ZeRO-3 gather with prefetch, ZeRO-2 buckets
 def test_zero3_unit_gather_with_prefetch_gives_every_unit_its_params():
     from fsdp_sharded_optimizer_step_gb300.zero3 import UnitGatherer
     sizes = [70001, 3, 65537, 12345, 9, 1 << 16, 777]
     c = SmallCase(sizes, 8, W.BF16, W.BF16, seed=41)
-    c.gpu_step(1)  # fills the param shards (and the full buffer, the reference here)
-    full = host_bits(c.full)
+    c.gpu_step(1)  # fills the param shards (and the full buffer)
+    assert c.oracle_step(1) == O.OK
+    c.assert_pshard_equal()  # the gatherer's input, checked against the oracle
+    full = c.out_o  # every unit's params in the oracle's full layout
     seen = {}
     gatherer = UnitGatherer(c.plan, c.pshard)
     for prefetch in (True, False):
@@ -542,8 +582,13 @@ def test_zero2_bucketed_reduce_scatter_then_shard_update_equals_fused_step():
 
     for u in reversed(range(len(sizes))):
         buckets.reduce(u, fill, b.gshard)
+    avg = O.avg_grad(b.g_o, O.BF16, b.pad)
+    assert np.array_equal(host_bits(b.gshard), f32bits(avg)[b.map])
     hp, _ = hp_for(1)
     Z.zero_adamw_shard_step(b.plan, b.gshard, b.master, b.m, b.v, hp, full=b.full)
+    assert b.oracle_step(1) == O.OK
+    b.assert_state_equal()
+    b.assert_full_equal()
     for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v), (a.full, b.full)):
         assert torch.equal(host_bits_t(x), host_bits_t(y))
 
