@@ -58,13 +58,15 @@ SYMBOLS = {}
 
 
 def lib():
-    """Loads the CUDA library (fails loudly when it is not built)."""
+    """Loads the CUDA library (fails loudly when it is not built).  ZERO_LIB in the
+    environment names another build of the same library (build.build_variant)."""
     global _LIB
     if _LIB is None:
-        if not os.path.exists(_build.LIB):
-            raise RuntimeError(f"CUDA library {_build.LIB} is missing: build it with "
+        path = os.environ.get("ZERO_LIB") or _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library {path} is missing: build it with "
                                "fsdp_sharded_optimizer_step_gb300.build.build() (or __graft_entry__.build())")
-        L = C.CDLL(_build.LIB)
+        L = C.CDLL(path)
         p, i32, i64, f32 = C.c_void_p, C.c_int32, C.c_int64, C.c_float
         pp = C.POINTER(C.c_void_p)
         sig = {
@@ -90,6 +92,11 @@ def lib():
             "zero_clip_reduce_unit": (C.c_int, [p, i32, pp, i32, pp, p]),
             "zero_clip_finalize": (C.c_int, [p, f32, p, p]),
             "zero_adamw_shard_step_clipped": (C.c_int, [p, pp, pp, pp, pp, pp, p, i32, p, i32, p]),
+            "zero_offload_create": (C.c_int, [p, i32, i64, C.POINTER(C.c_void_p)]),
+            "zero_offload_destroy": (None, [p]),
+            "zero_offload_adamw": (C.c_int, [p, pp, pp, pp, pp, pp, p, i32, p, C.c_double, i32]),
+            "zero_offload_step": (C.c_int, [p, pp, i32, pp, pp, pp, pp, pp, p, p, i32, p, p, p]),
+            "zero_offload_timings": (C.c_int, [p, p]),
             "zero_plan_device_errors": (C.c_int, [p, p, p]),
             "zero_plan_check": (C.c_int, [p, p]),
             "zero_debug_drop_copy": (C.c_int, [i64]),
@@ -368,9 +375,13 @@ def zero_grad_sqnorm_noalloc(grads, sqnorm_out, stream=None):
         raise ValueError(f"grads: dtype {rows[0].dtype} not allowed")
     if sqnorm_out.device != dev or sqnorm_out.dtype != torch.float64:
         raise ValueError("sqnorm_out: need a float64 tensor on the gradients' device")
+    if dev.type != "cuda":
+        raise ValueError("grads: need CUDA tensors")
     arr = (C.c_void_p * len(rows))(*[r.data_ptr() for r in rows])
-    _check(lib().zero_grad_sqnorm_noalloc(arr, len(rows), _DTYPES[rows[0].dtype], n, C.c_void_p(sqnorm_out.data_ptr()),
-                                          _stream(stream, dev)), "zero_grad_sqnorm_noalloc")
+    with torch.cuda.device(dev):  # the library works on the current device
+        _check(lib().zero_grad_sqnorm_noalloc(arr, len(rows), _DTYPES[rows[0].dtype], n,
+                                              C.c_void_p(sqnorm_out.data_ptr()), _stream(stream, dev)),
+               "zero_grad_sqnorm_noalloc")
 
 
 def zero_step_unit(plan, unit, grads_unit, master, m, v, hp: AdamW, full=None, pshard=None, stream=None):
@@ -443,3 +454,114 @@ def zero_all_gather_unit(plan, unit, shards, dst_unit, stream=None):
         raise ValueError("shards and dst_unit must have the same dtype")
     _check(lib().zero_all_gather_unit(plan.handle, int(unit), s, dp, sd, _stream(stream, plan.device)),
            "zero_all_gather_unit")
+
+
+# ------------------------------------------------------------------ ZeRO-Offload (host-resident state)
+def _host_rows(plan, x, length, what, dtypes):
+    """A [N, length] HOST tensor (or N 1-D host tensors) -> host array of N host pointers, dtype code."""
+    rows = list(x.unbind(0)) if isinstance(x, torch.Tensor) and x.dim() == 2 else list(x)
+    if len(rows) != plan.n_ranks:
+        raise ValueError(f"{what}: expected {plan.n_ranks} rank arrays, got {len(rows)}")
+    dt = rows[0].dtype
+    for r in rows:
+        if r.device.type != "cpu":
+            raise ValueError(f"{what}: host (CPU) tensors expected, got {r.device}")
+        if r.dtype != dt or dt not in dtypes:
+            raise ValueError(f"{what}: dtype {r.dtype} not allowed")
+        if r.dim() != 1 or not r.is_contiguous() or r.numel() != length:
+            raise ValueError(f"{what}: each rank array must be contiguous 1-D of {length} elements")
+    return (C.c_void_p * len(rows))(*[r.data_ptr() if r.numel() else 0 for r in rows]), _DTYPES[dt]
+
+
+def _host_one(x, length, what, dtypes):
+    if x.device.type != "cpu" or x.dtype not in dtypes or not x.is_contiguous() or x.numel() != length:
+        raise ValueError(f"{what}: need a contiguous {length}-element host tensor of {dtypes}")
+    return C.c_void_p(x.data_ptr()), _DTYPES[x.dtype]
+
+
+def zero_offload_create(plan, n_threads=0, batch_min=0):
+    h = C.c_void_p()
+    _check(lib().zero_offload_create(plan.handle, int(n_threads), int(batch_min), C.byref(h)), "zero_offload_create")
+    return h
+
+
+def zero_offload_destroy(handle):
+    lib().zero_offload_destroy(handle)
+
+
+def zero_offload_adamw(eng, gshard_h, master_h, m_h, v_h, hp: AdamW, full_h=None, pshard_h=None, sqnorm=0.0, unit=-1):
+    """The host-core update alone on host tensors (see include/zero.h); returns the status
+    (ZERO_OK, or ZERO_ENONFINITE when clipping with a non-finite S); other errors raise."""
+    plan = eng.plan
+    gs, _ = _host_rows(plan, gshard_h, plan.H, "gshard_h", _F)
+    W, _ = _host_rows(plan, master_h, plan.H, "master_h", _F)
+    M, _ = _host_rows(plan, m_h, plan.H, "m_h", _F)
+    V, _ = _host_rows(plan, v_h, plan.H, "v_h", _F)
+    pdt = None
+    fp = None
+    if full_h is not None:
+        fp, pdt = _host_one(full_h, plan.P_pad, "full_h", _G)
+    ps = None
+    if pshard_h is not None:
+        ps, d = _host_rows(plan, pshard_h, plan.H, "pshard_h", _G)
+        if pdt is not None and d != pdt:
+            raise ValueError("full_h and pshard_h must have the same dtype")
+        pdt = d
+    c = hp.c()
+    rc = lib().zero_offload_adamw(eng.handle, gs, W, M, V, ps, fp, ZERO_BF16 if pdt is None else pdt, C.byref(c),
+                                  float(sqnorm), int(unit))
+    if rc not in (ZERO_OK, ZERO_ENONFINITE):
+        _check(rc, "zero_offload_adamw")
+    return rc
+
+
+def zero_offload_step(eng, grads, gshard_dev, gshard_h, master_h, m_h, v_h, full_h, hp: AdamW, full_dev=None,
+                      stream=None):
+    """The offloaded step (see include/zero.h).  grads, gshard_dev: device [N, P_pad] / [N, H];
+    gshard_h, master_h, m_h, v_h: host [N, H] (pinned for overlap); full_h: host [P_pad];
+    full_dev: device [P_pad] or None.  Returns (status, S): status ZERO_OK or ZERO_ENONFINITE
+    (clipped step skipped), S the global sum of squares when clipping (else None)."""
+    plan = eng.plan
+    g, gd = _rows(plan, grads, plan.P_pad, "grads", _G)
+    gsd, _ = _rows(plan, gshard_dev, plan.H, "gshard_dev", _F)
+    gsh, _ = _host_rows(plan, gshard_h, plan.H, "gshard_h", _F)
+    W, _ = _host_rows(plan, master_h, plan.H, "master_h", _F)
+    M, _ = _host_rows(plan, m_h, plan.H, "m_h", _F)
+    V, _ = _host_rows(plan, v_h, plan.H, "v_h", _F)
+    fh, pdt = _host_one(full_h, plan.P_pad, "full_h", _G)
+    fd = None
+    if full_dev is not None:
+        fd, d = _one(plan, full_dev, plan.P_pad, "full_dev", _G)
+        if d != pdt:
+            raise ValueError("full_h and full_dev must have the same dtype")
+    c = hp.c()
+    S = C.c_double(float("nan"))
+    with torch.cuda.device(plan.device):
+        rc = lib().zero_offload_step(eng.handle, g, gd, gsd, gsh, W, M, V, fh, fd, pdt, C.byref(c), C.byref(S),
+                                     _stream(stream, plan.device))
+    if rc not in (ZERO_OK, ZERO_ENONFINITE):
+        _check(rc, "zero_offload_step")
+    return rc, (S.value if hp.max_norm > 0 else None)
+
+
+def zero_offload_timings(eng):
+    """Last step's timings (ms): call, waiting for gradient slices, host update, device time to
+    the last param copy, device time to the last gradient slice (see include/zero.h)."""
+    ms = (C.c_double * 5)()
+    _check(lib().zero_offload_timings(eng.handle, ms), "zero_offload_timings")
+    return dict(call_ms=ms[0], wait_ms=ms[1], update_ms=ms[2], device_to_params_ms=ms[3],
+                device_to_grads_ms=ms[4])
+
+
+class OffloadEngine:
+    """Owns a zero_offload engine for a plan (host worker threads; copy streams on first step)."""
+
+    def __init__(self, plan, n_threads=0, batch_min=0):
+        self.plan = plan  # the engine keeps a pointer to the plan: hold it as long
+        self.handle = zero_offload_create(plan, n_threads, batch_min)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and _LIB is not None:
+            zero_offload_destroy(h)
+            self.handle = None

@@ -76,6 +76,24 @@ static int seg_range(const zero_plan *plan, int32_t unit, int64_t &begin, int64_
 
 static bool valid_dtype(int32_t d) { return d == ZERO_BF16 || d == ZERO_F32; }
 
+int reduce_units(const zero_plan *plan, int32_t u0, int32_t u1, const void *const *grads, int32_t gdtype,
+                 float *const *gshard, bool want_partials, cudaStream_t st) {
+    if (u0 < 0 || u1 > plan->n_units || u0 > u1) return ZERO_EINVAL;
+    const int64_t begin = plan->unit_seg_begin[u0];
+    const int64_t count = plan->unit_seg_begin[u1] - begin;
+    if (count == 0) return ZERO_OK;
+    KParams kp;
+    fill_common(plan, kp);
+    kp.seg_base = begin;
+    kp.write_g = 1;
+    kp.want_partials = want_partials ? 1 : 0;
+    for (int q = 0; q < plan->n_ranks; ++q) {
+        kp.grads[q] = grads[q];
+        kp.gshard[q] = gshard[q];
+    }
+    return launch_pipe(MODE_REDUCE, gdtype, count, kp, st);
+}
+
 }  // namespace zero
 
 using namespace zero;

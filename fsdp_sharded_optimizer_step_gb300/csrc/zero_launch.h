@@ -66,4 +66,11 @@ int launch_gather(int64_t count, const KParams &kp, cudaStream_t st);
 // Testing aid: the next pipelined launch skips the copies of tile `tile` of its first segment.
 void arm_drop_tile(int64_t tile);
 
+// Reduce-scatter + average of units [u0, u1) from full-length gradient rows into
+// the fp32 gradient shard, one launch; with want_partials also the units'
+// per-segment sums of squares (at their table positions in the workspace).
+// The plan must be attached to the current device (checked by the caller).
+int reduce_units(const zero_plan *plan, int32_t u0, int32_t u1, const void *const *grads, int32_t gdtype,
+                 float *const *gshard, bool want_partials, cudaStream_t st);
+
 }  // namespace zero

@@ -297,6 +297,97 @@ int zero_adamw_shard_step_clipped(const zero_plan *plan, const float *const *gsh
 int zero_reshard(const zero_plan *from, const zero_plan *to, const void *const *src, void *const *dst,
                  int32_t dtype, zero_stream_t stream);
 
+/* ---------------------------------------------------------------- ZeRO-Offload: the update on the host cores */
+
+/* ZeRO-Offload ("Learn: ZeRO & FSDP", section 6, Offloading; "ZeRO and FSDP
+ * sharding", Implementation notes): the optimizer state and the fp32 AdamW
+ * step move to host memory and the host CPU.  The GPU reduce-scatters the
+ * gradients, the averaged fp32 gradient shard goes down to the host, the host
+ * cores run the update, and the updated params come back.  It trades the host
+ * link's bandwidth for device memory: master, m and v (12 bytes per parameter)
+ * never occupy HBM.
+ *
+ * An engine owns a pool of host worker threads and, from its first step on,
+ * two copy streams and a few events on the plan's device.  The results are
+ * those of zero_step, bit for bit: every element goes through the operations
+ * listed at the top of this header, each one binary32 operation rounded to
+ * nearest even (the host code is compiled without contraction and runs the
+ * update in the default floating-point environment, subnormals kept).
+ *   plan        the layout (it must outlive the engine; zero_offload_step
+ *               needs it attached).
+ *   n_threads   host threads of the update (>= 1), or 0 for every core this
+ *               process may run on.
+ *   batch_min   the step is pipelined over batches of consecutive units of at
+ *               least this many padded elements; 0 picks 2^22.
+ * Host only; needs no GPU.  Errors: ZERO_EINVAL, ZERO_ENOMEM. */
+typedef struct zero_offload zero_offload;
+int zero_offload_create(const zero_plan *plan, int32_t n_threads, int64_t batch_min, zero_offload **out);
+
+/* Frees the engine (threads, copy streams, events).  NULL is a no-op. */
+void zero_offload_destroy(zero_offload *eng);
+
+/* The update on the host cores alone, on HOST arrays (no GPU involved): for
+ * every rank r and every shard position of unit `unit` (-1: all units), AdamW
+ * with the averaged gradient gshard_h[r][j] on master_h/m_h/v_h[r][j].
+ *   gshard_h   [N] host fp32 arrays of H elements (read only).
+ *   master_h, m_h, v_h  [N] host fp32 arrays of H elements, updated in place.
+ *   pshard_h   [N] host arrays of H elements of pdtype, or NULL: the param shards.
+ *   full_h     a host array of P_pad elements of pdtype, or NULL: the params
+ *              at their full positions (F_u + r h_u + j).
+ *   sqnorm     used only when hp->max_norm > 0: the sum of squares S of the
+ *              averaged gradient; the gradient is scaled by min(1, max_norm /
+ *              (sqrt(S) + 1e-6)) (binary64, rounded once to binary32) first,
+ *              as zero_step does; S not finite returns ZERO_ENONFINITE before
+ *              anything is touched.
+ * Synchronous: the engine's threads share the positions out.
+ * Errors: ZERO_EINVAL, ZERO_ENONFINITE, ZERO_ENOMEM. */
+int zero_offload_adamw(zero_offload *eng, const float *const *gshard_h, float *const *master_h, float *const *m_h,
+                       float *const *v_h, void *const *pshard_h, void *full_h, int32_t pdtype, const zero_hparams *hp,
+                       double sqnorm, int32_t unit);
+
+/* The offloaded step, pipelined over the engine's batches of units:
+ *   1. GPU (`stream`): reduce-scatter + average of the batch's units from the N
+ *      device gradient buffers into gshard_dev (with clipping also the batch's
+ *      sums of squares);
+ *   2. GPU copy stream: the batch's slices of gshard_dev to gshard_h;
+ *   3. host cores: AdamW of the batch on master_h/m_h/v_h as soon as its slices
+ *      have landed, the params written to full_h;
+ *   4. GPU copy stream: the batch's params from full_h to full_dev;
+ * so copies down, host updates and copies up of different batches overlap.
+ * With clipping (hp->max_norm > 0) the norm passes of all batches run first, S
+ * is read back (the one wait for the GPU), then the updates run as above; S not
+ * finite skips the update (master_h, m_h, v_h, full_h and full_dev are left
+ * untouched), returns ZERO_ENONFINITE, and is also reported by a later
+ * zero_plan_check, as for zero_step.
+ *   grads       [N] DEVICE buffers of P_pad elements of gdtype, read only.
+ *   gshard_dev  [N] DEVICE fp32 buffers of H elements: staging.
+ *   gshard_h    [N] HOST fp32 arrays of H elements: staging.
+ *   master_h, m_h, v_h  [N] HOST fp32 arrays of H elements: the optimizer state.
+ *   full_h      a HOST array of P_pad elements of pdtype: receives the params.
+ *   full_dev    a DEVICE buffer of P_pad elements of pdtype, or NULL.
+ *   sqnorm_out  a HOST binary64 receiving S when clipping, or NULL.
+ * Host arrays should be page-locked (cudaHostAlloc, a pinned torch tensor) so
+ * that the copies run asynchronously; pageable memory gives the same results
+ * with copies that block.  The call returns when the host update is done and
+ * the last param copy is queued; `stream` is made to wait for every copy, so
+ * work queued on it afterwards sees full_dev updated and may overwrite
+ * gshard_dev.  The plan must be attached to the current device; calls with one
+ * engine or one plan must not overlap.  After ZERO_ECUDA the step may be
+ * partly done.  Errors: ZERO_EINVAL, ZERO_EALIGN (device pointers),
+ * ZERO_ENOTATTACHED, ZERO_ECUDA, ZERO_ENONFINITE, ZERO_ENOMEM. */
+int zero_offload_step(zero_offload *eng, const void *const *grads, int32_t gdtype, float *const *gshard_dev,
+                      float *const *gshard_h, float *const *master_h, float *const *m_h, float *const *v_h,
+                      void *full_h, void *full_dev, int32_t pdtype, const zero_hparams *hp, double *sqnorm_out,
+                      zero_stream_t stream);
+
+/* Timings of the engine's last zero_offload_step in milliseconds (waits for
+ * its copies to finish): ms[0] host time inside the call; ms[1] host time spent
+ * waiting for gradient slices to land (and, clipping, for S); ms[2] host time
+ * spent updating; ms[3] device time from the step's start until its last param
+ * copy had landed; ms[4] device time from the start until its last gradient
+ * slice had landed on the host.  ZERO_EINVAL before the first step. */
+int zero_offload_timings(zero_offload *eng, double *ms);
+
 /* ---------------------------------------------------------------- without allocation */
 
 /* No counterpart on the pages: an addition for callers that cannot allocate
@@ -315,16 +406,26 @@ int zero_reshard(const zero_plan *from, const zero_plan *to, const void *const *
  * values (256 KB) compiled into the library, which every GPU that loads the
  * library holds until the process exits.
  *   grads     [n_ranks] device pointers to n elements of gdtype each (aligned
- *             to the element size).
+ *             to the element size), on the current device.  With n == 0 they
+ *             may be NULL.
  *   n         0 <= n <= ZERO_NOALLOC_MAX_CHUNKS * ZERO_NOALLOC_CHUNK
  *             (2^32 elements); larger n returns ZERO_ERANGE before any launch.
- *   sqnorm_dev  DEVICE binary64 receiving S (8-byte aligned), asynchronously.
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  All calls share the one array (it keeps the last call's
- * partials, and every call overwrites the ones it reads), so calls whose work
- * overlaps on the GPU -- on two streams, or from two threads -- race; order them
- * on one stream. */
+ *             n == 0 writes S = 0.
+ *   sqnorm_dev  DEVICE binary64 receiving S (8-byte aligned), asynchronously,
+ *             on the current device.
+ * A gradient that is inf or NaN makes S inf or NaN (a watchdog tests S).
+ * Set-up: the first call on each device, with that device current, loads the
+ * library's norm kernels onto the device and looks up the array's device
+ * address (cudaGetSymbolAddress); the address is cached for the life of the
+ * process, so the device's context must not be reset (cudaDeviceReset) after
+ * it.  Loading code takes device memory, so make that first call -- a call
+ * with n = 0 is enough -- while device memory is still free, and before any
+ * stream capture; later calls take no device memory at all.
+ * All calls share the one array (it keeps the last call's partials, and every
+ * call overwrites the ones it reads), so calls whose work overlaps on the GPU
+ * -- on two streams, or from two threads -- race; order them on one stream.
+ * Errors: ZERO_EINVAL (NULL, n < 0, n_ranks out of range, a pointer that is not
+ * device memory of the current device), ZERO_EALIGN, ZERO_ERANGE, ZERO_ECUDA. */
 #define ZERO_NOALLOC_CHUNK 131072
 #define ZERO_NOALLOC_MAX_CHUNKS 32768
 int zero_grad_sqnorm_noalloc(const void *const *grads, int32_t n_ranks, int32_t gdtype, int64_t n,
