@@ -330,6 +330,86 @@ def update_bytes_per_element(cfg):
 E2E_PINNED_BUDGET = 32e9
 
 
+SECONDARY = ("4b_z3", "1p3b_clip", "finewrap")
+
+
+def run_secondary(name, steps, warmup, dev):
+    """One of the other full-size workloads on this GPU: its whole step timed with CUDA events
+    (inputs resident in HBM, larger than L2), the update launch(es) timed on their own, and the
+    roofline of each against the measured HBM copy peak.  ZeRO-3 (4b_z3): the fused update writes
+    the ranks' param shards (42 B/element) and 33 per-unit all-gathers fill the full buffer
+    (4 B/element more: 46 B/element for the whole step)."""
+    import fsdp_sharded_optimizer_step_gb300 as Z
+    from fsdp_sharded_optimizer_step_gb300 import workloads as W
+    cfg = W.CONFIGS[name]
+    sizes = cfg["units"]()
+    N = cfg["N"]
+    plan = Z.ZeroPlan(sizes, N, dev)
+    P, H = plan.P_pad, plan.H
+    gdt = torch.bfloat16 if cfg["gdtype"] == W.BF16 else torch.float32
+    pdt = torch.bfloat16 if cfg["pdtype"] == W.BF16 else torch.float32
+    grads = W.make_grads(N, P, cfg["gdtype"], sigma=cfg.get("grad_sigma", 1e-3), device=dev, seed=1,
+                         outlier_frac=cfg.get("outlier_frac", 0.0), outlier_scale=cfg.get("outlier_scale", 1.0),
+                         out=Z.rank_buffers(N, P, gdt, dev))
+    master, m, v = W.make_state(N, H, sigma=cfg.get("master_sigma", 0.02), device=dev,
+                                out=tuple(Z.rank_buffers(N, H, torch.float32, dev) for _ in range(3)))
+    clip = cfg.get("max_norm", 0.0) > 0
+    z3 = cfg["stage"] == 3
+    full = torch.zeros(P, dtype=pdt, device=dev)
+    pshard = Z.rank_buffers(N, H, pdt, dev, zero=True) if z3 else None
+    gshard = Z.rank_buffers(N, H, torch.float32, dev) if clip else None
+    sq = torch.zeros(1, dtype=torch.float64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(t, ev=None):
+        hp = Z.AdamW(t=t, max_norm=cfg.get("max_norm", 0.0), **W.HP)
+        if ev is not None:
+            ev[0].record(stream)
+        Z.zero_step(plan, grads, master, m, v, hp, full=None if z3 else full, pshard=pshard, gshard_ws=gshard,
+                    sqnorm_out=sq if clip else None)
+        if ev is not None:
+            ev[1].record(stream)
+        if z3:
+            for u in range(plan.n_units):
+                Z.zero_all_gather_bf16(plan, pshard, full, unit=u)
+
+    for t in range(1, warmup + 1):
+        step(t)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    clocks.begin()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(steps):
+        step(warmup + 1 + k, evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.end()
+    clock_info = clocks.stop()
+    ms = t0.elapsed_time(t1) / steps
+    upd_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    peak, peak_kind = measured_hbm_peak()
+    bpe = update_bytes_per_element(cfg)
+    upd_gbs = bpe * P / (upd_ms / 1e3) / 1e9
+    traffic = ncu_traffic(name, "clip" if clip else "fused")
+    out = {"workload": f"{name}: {cfg['desc']}", "psi": int(sum(sizes)), "p_pad": P, "steps": steps, "warmup": warmup,
+           "ms_per_step": ms, "params_per_s": int(sum(sizes)) / (ms / 1e3),
+           "gpu_launches_per_step": (3 if clip else 1) + (plan.n_units if z3 else 0),
+           "update": {"kernel": "k_pipe<REDUCE> + k_finalize + k_pipe<SHARD>" if clip else "k_pipe<FUSED>",
+                      "ms": upd_ms, "bytes_per_element": bpe,
+                      "roofline": {"bound": "hbm", "achieved": upd_gbs, "peak": peak, "unit": "GB/s",
+                                   "frac": upd_gbs / peak, "traffic": traffic, "peak_kind": peak_kind}},
+           "clocks": clock_info}
+    step_bpe = bpe + (4 if z3 else 0)  # ZeRO-3: + the per-unit gathers (2 B read + 2 B written per element)
+    step_gbs = step_bpe * P / (ms / 1e3) / 1e9
+    out["step_roofline"] = {"bound": "hbm", "achieved": step_gbs, "peak": peak, "unit": "GB/s", "frac": step_gbs / peak,
+                            "pct_of_8tbs_nominal": 100 * step_gbs / 8000.0, "bytes_per_element": step_bpe,
+                            "peak_kind": peak_kind}
+    return out
+
+
 def measure_e2e(args, world, dev, stream, grads, full, step, N, P, gdt, pdt, psi, plan=None, state=None, streamed=False,
                 max_norm=0.0, gshard=None):
     """Same metric through the public API with host buffers: every step takes the
@@ -492,6 +572,156 @@ def run_gather(args, world, rank, local):
     return 0
 
 
+def run_offload(args, world, rank, local):
+    """ZeRO-Offload step (zero_offload_step): gradients in HBM, master/m/v in pinned host
+    memory, the GPU reduce-scatters batch by batch, the host cores run AdamW as each
+    batch's gradient shard lands, the bf16 params go back to HBM.  Reports params/s,
+    the host link's rates, the host cores' update rate, and where a step's time goes."""
+    import fsdp_sharded_optimizer_step_gb300 as Z
+    from fsdp_sharded_optimizer_step_gb300 import binding as B
+    from fsdp_sharded_optimizer_step_gb300 import build as zbuild
+    from fsdp_sharded_optimizer_step_gb300 import workloads as W
+    zbuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = W.CONFIGS[args.config]
+    sizes = cfg["units"]()
+    N = cfg["N"]
+    plan = Z.ZeroPlan(sizes, N, dev)
+    P, H = plan.P_pad, plan.H
+    gdt = torch.bfloat16 if cfg["gdtype"] == W.BF16 else torch.float32
+    pdt = torch.bfloat16 if cfg["pdtype"] == W.BF16 else torch.float32
+    grads = W.make_grads(N, P, cfg["gdtype"], sigma=cfg.get("grad_sigma", 1e-3), device=dev, seed=1 + 100 * rank,
+                         outlier_frac=cfg.get("outlier_frac", 0.0), outlier_scale=cfg.get("outlier_scale", 1.0),
+                         out=Z.rank_buffers(N, P, gdt, dev))
+    state_dev = W.make_state(N, H, sigma=cfg.get("master_sigma", 0.02), device=dev)
+    host = []
+    for x in state_dev:
+        h = torch.empty(N, H, dtype=torch.float32, pin_memory=True)
+        h.copy_(x)
+        host.append(h)
+    master_h, m_h, v_h = host
+    del state_dev
+    torch.cuda.empty_cache()
+    gshard_dev = Z.rank_buffers(N, H, torch.float32, dev)
+    gshard_h = torch.empty(N, H, dtype=torch.float32, pin_memory=True)
+    full_h = torch.empty(P, dtype=pdt, pin_memory=True)
+    full_dev = torch.empty(P, dtype=pdt, device=dev)
+    eng = B.OffloadEngine(plan, n_threads=args.offload_threads, batch_min=args.offload_batch)
+    threads = args.offload_threads or len(os.sched_getaffinity(0))
+    stream = torch.cuda.current_stream(dev)
+    max_norm = cfg.get("max_norm", 0.0)
+
+    def step(t):
+        hp = Z.AdamW(t=t, max_norm=max_norm, **W.HP)
+        rc, _ = Z.zero_offload_step(eng, grads, gshard_dev, gshard_h, master_h, m_h, v_h, full_h, hp,
+                                    full_dev=full_dev, stream=stream)
+        if rc != B.ZERO_OK:
+            raise RuntimeError(f"zero_offload_step returned {rc}")
+
+    for t in range(1, args.warmup + 1):
+        step(t)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    clocks.begin()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    e0.record(stream)
+    for k in range(args.steps):
+        step(args.warmup + 1 + k)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall_ms = (time.perf_counter() - w0) * 1e3 / args.steps
+    clocks.end()
+    clock_info = clocks.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    psi = int(sum(sizes))
+    # one more step, for the breakdown of where its time goes
+    step(args.warmup + args.steps + 1)
+    tm = Z.zero_offload_timings(eng)
+    # the pieces alone: the host link each way, and the host cores' update
+    d2h_bytes, h2d_bytes = 4 * N * H, P * full_h.element_size()
+
+    def copy_ms(dst, src, reps=3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        dst.copy_(src, non_blocking=True)
+        a.record(stream)
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / reps
+
+    t_d2h = copy_ms(gshard_h, gshard_dev)
+    t_h2d = copy_ms(full_dev, full_h)
+    hp = Z.AdamW(t=1, **W.HP)
+    reps = 3
+    Z.zero_offload_adamw(eng, gshard_h, master_h, m_h, v_h, hp, full_h=full_h)
+    c0 = time.perf_counter()
+    for _ in range(reps):
+        Z.zero_offload_adamw(eng, gshard_h, master_h, m_h, v_h, hp, full_h=full_h)
+    t_host = (time.perf_counter() - c0) * 1e3 / reps
+    host_bytes = N * H * (4 + 12 + 12) + P * full_h.element_size()
+    host_peak = host_stream_gbps(threads)
+    if rank == 0:
+        print(json.dumps({
+            "metric": "ZeRO-Offload step params/sec (state in host memory, update on the host cores)",
+            "value": world * psi / (ms / 1e3), "unit": "params/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "wall_ms_per_step": wall_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": dict(workload_config(args.config, cfg, plan), host_threads=threads,
+                           batches=len(eng_batches(plan, args.offload_batch))),
+            "link": {"d2h_bytes_per_step": d2h_bytes, "h2d_bytes_per_step": h2d_bytes,
+                     "d2h_GBps_alone": d2h_bytes / (t_d2h / 1e3) / 1e9, "h2d_GBps_alone": h2d_bytes / (t_h2d / 1e3) / 1e9,
+                     "d2h_ms_alone": t_d2h, "h2d_ms_alone": t_h2d},
+            "host_update": {"ms_alone": t_host, "params_per_s": psi / (t_host / 1e3),
+                            "bytes_per_step": host_bytes, "GBps": host_bytes / (t_host / 1e3) / 1e9,
+                            "threads": threads, "host_stream_add_GBps": host_peak,
+                            "frac_of_host_stream": host_bytes / (t_host / 1e3) / 1e9 / host_peak},
+            "breakdown_one_step_ms": tm,
+            "share": {"update_on_cores": tm["update_ms"] / tm["device_to_params_ms"],
+                      "waiting_for_link": tm["wait_ms"] / tm["device_to_params_ms"]},
+            "gpu_launches": args.steps * len(eng_batches(plan, args.offload_batch)) * (2 if max_norm > 0 else 1),
+            "clocks": clock_info}), flush=True)
+    return 0
+
+
+def host_stream_gbps(threads, n=1 << 28, reps=5):
+    """The host's memory bandwidth as a STREAM-style add, z = x + y over three fp32
+    arrays of n elements (12 bytes per element) on `threads` torch threads: the
+    reference the offloaded update's host traffic is set against."""
+    old = torch.get_num_threads()
+    torch.set_num_threads(threads)
+    try:
+        x, y, z = torch.ones(n), torch.ones(n), torch.empty(n)
+        torch.add(x, y, out=z)
+        best = float("inf")
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            torch.add(x, y, out=z)
+            best = min(best, time.perf_counter() - t0)
+        return 12 * n / best / 1e9
+    finally:
+        torch.set_num_threads(old)
+
+
+def eng_batches(plan, batch_min):
+    """The engine's batches of consecutive units (at least batch_min padded elements each,
+    2^22 when 0), as the library forms them; for reporting the launch count."""
+    bmin = batch_min or (1 << 22)
+    out, u, U = [], 0, plan.n_units
+    while u < U:
+        u0, elems = u, 0
+        while u < U and (elems < bmin or plan.S[u] == 0):
+            elems += plan.S[u]
+            u += 1
+        if elems:
+            out.append((u0, u))
+    return out
+
+
 def _time_ms(fn, stream, reps):
     fn()
     torch.cuda.synchronize()
@@ -548,37 +778,46 @@ def run_unit_flows(args, world, rank, local):
         out.update(metric="ZeRO-3 forward timeline: per-unit gather + synthetic GEMM (ms per pass)",
                    value=best, unit="ms", higher_is_better=False, timeline=timeline)
     else:
+        from fsdp_sharded_optimizer_step_gb300.zero3 import BucketedStep
         grads = W.make_grads(N, P, W.BF16, device=dev, out=Z.rank_buffers(N, P, torch.bfloat16, dev))
         master, m, v = W.make_state(N, H, device=dev,
                                     out=tuple(Z.rank_buffers(N, H, torch.float32, dev) for _ in range(3)))
         gshard = Z.rank_buffers(N, H, torch.float32, dev)
         full = torch.zeros(P, dtype=torch.bfloat16, device=dev)
-        buckets = BucketedReduceScatter(plan)
         hp = Z.AdamW(t=1, **W.HP)
-
-        def fill(u, view):  # the backward of unit u: here its gradients already exist
-            view.copy_(grads[:, plan.F[u]:plan.F[u] + plan.S[u]])
-
-        def bucketed():
-            for u in reversed(range(plan.n_units)):
-                buckets.reduce(u, fill, gshard)
-            Z.zero_adamw_shard_step(plan, gshard, master, m, v, hp, full=full)
-
-        def rs_units():
-            for u in reversed(range(plan.n_units)):
-                Z.zero_reduce_scatter_unit(plan, u, buckets.bucket[:, :plan.S[u]], gshard)
-
-        t_bucketed = _time_ms(bucketed, stream, reps)
-        t_fill = _time_ms(lambda: [fill(u, buckets.bucket[:, :plan.S[u]]) for u in range(plan.n_units)], stream, reps)
-        t_rs = _time_ms(rs_units, stream, reps)
-        t_shard = _time_ms(lambda: Z.zero_adamw_shard_step(plan, gshard, master, m, v, hp, full=full), stream, reps)
         t_fused = _time_ms(lambda: Z.zero_step(plan, grads, master, m, v, hp, full=full), stream, reps)
-        out.update(metric="ZeRO-2 bucketed gradient flow: per-unit reduce-scatter + shard update (ms per step)",
-                   value=t_rs + t_shard, unit="ms", higher_is_better=False,
-                   flow={"bucketed_total_ms_incl_fill": t_bucketed, "fill_copies_ms": t_fill,
-                         "reduce_scatter_per_unit_ms": t_rs, "shard_update_ms": t_shard, "fused_step_ms": t_fused,
-                         "bucket_bytes": buckets.bucket_bytes, "full_gradient_bytes": N * P * 2,
-                         "gradient_shard_bytes": N * H * 4})
+
+        def fill(u0, u1, view):  # the backward of units [u0, u1): here their gradients already exist
+            view.copy_(grads[:, plan.F[u0]:plan.F[u0] + view.shape[1]])
+
+        flows = {}
+        for label, be in (("one unit per bucket", 1), ("2^26-element buckets", 1 << 26),
+                          ("default buckets", None), ("2^28-element buckets", 1 << 28)):
+            bs = BucketedStep(plan, bucket_elems=be)
+            first = bs.buckets[0]
+            fill(*first, bs.view(*first))
+
+            def updates():  # the bucket updates alone, back to back (the bucket holds gradients)
+                for u0, u1 in bs.buckets:
+                    Z.zero_step_units(plan, u0, u1, bs.view(u0, u1), master, m, v, hp, full=full)
+
+            flows[label] = {"buckets": len(bs.buckets), "bucket_bytes": bs.bucket_bytes,
+                            "bucket_updates_ms": _time_ms(updates, stream, reps),
+                            "total_ms_incl_fill_copies": _time_ms(
+                                lambda: bs.step(fill, master, m, v, hp, full=full), stream, reps)}
+            del bs
+        # the previous flow: per-unit reduce-scatter into the fp32 gradient shard, then the shard update
+        buckets = BucketedReduceScatter(plan)
+        t_rs = _time_ms(lambda: [Z.zero_reduce_scatter_unit(plan, u, buckets.bucket[:, :plan.S[u]], gshard)
+                                 for u in reversed(range(plan.n_units))], stream, reps)
+        t_shard = _time_ms(lambda: Z.zero_adamw_shard_step(plan, gshard, master, m, v, hp, full=full), stream, reps)
+        best = flows["default buckets"]["bucket_updates_ms"]
+        out.update(metric="ZeRO-2 bucketed step: bucket updates of the default bucketing (ms per step)",
+                   value=best, unit="ms", higher_is_better=False,
+                   flow={"fused_step_ms": t_fused, "bucketed": flows,
+                         "vs_fused": best / t_fused,
+                         "shard_route_ms": {"reduce_scatter_per_unit": t_rs, "shard_update": t_shard},
+                         "full_gradient_bytes": N * P * 2, "gradient_shard_bytes": N * H * 4})
     if rank == 0:
         print(json.dumps(out), flush=True)
     return 0
@@ -597,11 +836,19 @@ def main():
                          "region (removes host launch overhead; the step counter t is the one captured)")
     ap.add_argument("--ref-sample", type=int, default=1 << 22)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--op", default="step", choices=["step", "reshard", "gather", "zero3_gather", "zero2_buckets"],
+    ap.add_argument("--secondary", action=argparse.BooleanOptionalAction, default=True,
+                    help="with the default gpt2l step on one GPU, also time the 4b_z3, 1p3b_clip and finewrap "
+                         "workloads (each after the previous one's buffers are freed) into a 'secondary' block")
+    ap.add_argument("--secondary-steps", type=int, default=5)
+    ap.add_argument("--offload-threads", type=int, default=0, help="host threads of the offloaded update (0: all)")
+    ap.add_argument("--offload-batch", type=int, default=0, help="offload pipeline batch, padded elements (0: 2^22)")
+    ap.add_argument("--op", default="step",
+                    choices=["step", "reshard", "gather", "zero3_gather", "zero2_buckets", "offload"],
                     help="step: the sharded optimizer step (default); reshard: checkpoint resharding of the state; "
                          "gather: the all-gather of every unit in one launch; "
                          "zero3_gather: per-unit gathers with/without prefetch beside a synthetic per-unit GEMM; "
-                         "zero2_buckets: bucketed reduce-scatter + shard update against the fused step")
+                         "zero2_buckets: the bucketed ZeRO-2 step against the fused step; "
+                         "offload: the ZeRO-Offload step with the state in host memory")
     ap.add_argument("--to-ranks", type=int, default=0, help="reshard target rank count (default 2N)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -615,6 +862,8 @@ def main():
         return run_gather(args, world, rank, local)
     if args.op in ("zero3_gather", "zero2_buckets"):
         return run_unit_flows(args, world, rank, local)
+    if args.op == "offload":
+        return run_offload(args, world, rank, local)
 
     import fsdp_sharded_optimizer_step_gb300 as Z
     from fsdp_sharded_optimizer_step_gb300 import build as zbuild
@@ -720,6 +969,17 @@ def main():
         e2e = {"value": None, "unit": UNIT, "skipped": f"{pinned_bytes / 1e9:.0f} GB of pinned host buffers "
                                                        f"exceeds the {E2E_PINNED_BUDGET / 1e9:.0f} GB budget"}
 
+    # ---------------- the other full-size workloads, each measured after this one's buffers are freed
+    secondary = None
+    if world == 1 and args.secondary and args.config == "gpt2l" and not (args.per_unit or args.graph):
+        del step, grads, master, m, v, full, pshard, gshard, sq, graph
+        plan = None
+        torch.cuda.empty_cache()
+        secondary = {}
+        for name in SECONDARY:
+            secondary[name] = run_secondary(name, args.secondary_steps, 3, dev)
+            torch.cuda.empty_cache()
+
     # ---------------- CPU oracle baseline (rank 0, one GPU only)
     cpu = cpu_all = None
     if rank == 0 and world == 1:
@@ -749,6 +1009,7 @@ def main():
                 "hbm_gbs": achieved, "pct_of_peak": 100 * achieved / peak,
                 "pct_of_8tbs_nominal": 100 * achieved / 8000.0,
                 "roofline": roofline, "cpu_baseline": cpu, "cpu_all_cores": cpu_all, "e2e": e2e,
+                "secondary": secondary,
                 "gpu_launches": args.steps * launches_per_step, "clocks": clock_info,
                 "kernel_source_sha256_16": kernel_source_hash(),
                 "device": torch.cuda.get_device_name(dev)}

@@ -86,6 +86,8 @@ def lib():
             "zero_step": (C.c_int, [p, pp, i32, pp, pp, pp, p, pp, i32, pp, p, p, i32, p]),
             "zero_grad_sqnorm_noalloc": (C.c_int, [pp, i32, i32, i64, p, p]),
             "zero_step_unit": (C.c_int, [p, i32, pp, i32, pp, pp, pp, p, pp, i32, p, p]),
+            "zero_step_units": (C.c_int, [p, i32, i32, pp, i32, pp, pp, pp, p, pp, i32, p, p]),
+            "zero_clip_reduce_units": (C.c_int, [p, i32, i32, pp, i32, pp, p]),
             "zero_reshard": (C.c_int, [p, p, pp, pp, i32, p]),
             "zero_all_gather_unit": (C.c_int, [p, i32, pp, p, i32, p]),
             "zero_reduce_scatter_unit": (C.c_int, [p, i32, pp, i32, pp, f32, p]),
@@ -394,6 +396,33 @@ def zero_step_unit(plan, unit, grads_unit, master, m, v, hp: AdamW, full=None, p
     c = hp.c()
     _check(lib().zero_step_unit(plan.handle, int(unit), g, gd, W, M, V, fp, ps, pdt, C.byref(c),
                                 _stream(stream, plan.device)), "zero_step_unit")
+
+
+def _bucket_len(plan, u0, u1):
+    if not (0 <= u0 < u1 <= plan.n_units):
+        raise ValueError(f"unit range [{u0}, {u1}) outside [0, {plan.n_units})")
+    return (plan.F[u1] if u1 < plan.n_units else plan.P_pad) - plan.F[u0]
+
+
+def zero_step_units(plan, u0, u1, grads_bucket, master, m, v, hp: AdamW, full=None, pshard=None, stream=None):
+    """The fused step for units [u0, u1) from bucket-local gradient buffers (rank q's padded
+    positions F_u0 .. F_u1 - 1), one launch."""
+    g, gd = _rows(plan, grads_bucket, _bucket_len(plan, u0, u1), "grads_bucket", _G)
+    W, _ = _rows(plan, master, plan.H, "master", _F)
+    M, _ = _rows(plan, m, plan.H, "m", _F)
+    V, _ = _rows(plan, v, plan.H, "v", _F)
+    fp, ps, pdt = _outputs(plan, full, pshard)
+    c = hp.c()
+    _check(lib().zero_step_units(plan.handle, int(u0), int(u1), g, gd, W, M, V, fp, ps, pdt, C.byref(c),
+                                 _stream(stream, plan.device)), "zero_step_units")
+
+
+def zero_clip_reduce_units(plan, u0, u1, grads_bucket, gshard, stream=None):
+    """Clipped step, pass 1 for units [u0, u1) from a bucket-local gradient buffer."""
+    g, gd = _rows(plan, grads_bucket, _bucket_len(plan, u0, u1), "grads_bucket", _G)
+    gs, _ = _rows(plan, gshard, plan.H, "gshard", _F)
+    _check(lib().zero_clip_reduce_units(plan.handle, int(u0), int(u1), g, gd, gs, _stream(stream, plan.device)),
+           "zero_clip_reduce_units")
 
 
 def zero_reduce_scatter_unit(plan, unit, grads_unit, gshard, coef=1.0, stream=None):

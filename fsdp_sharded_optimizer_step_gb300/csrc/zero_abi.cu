@@ -298,26 +298,36 @@ extern "C" int zero_step(const zero_plan *plan, const void *const *grads, int32_
     return launch_pipe(MODE_SHARD, ZERO_F32, count, kp, st);
 }
 
-// Unit-local variants: grads_unit[q] holds only unit u's S_u padded
-// gradient positions (element i = full position F_u + i).
-static int unit_common(const zero_plan *plan, int32_t unit, const void *const *grads_unit, int32_t gdtype,
-                       int64_t &begin, int64_t &count, KParams &kp) {
+// Bucket-local variants: grads_b[q] holds only the padded gradient positions
+// of units [u0, u1), element i = full position F_u0 + i (one unit: u1 = u0 + 1).
+static int units_common(const zero_plan *plan, int32_t u0, int32_t u1, const void *const *grads_b, int32_t gdtype,
+                        int64_t &begin, int64_t &count, KParams &kp) {
     int rc = check_attached(plan);
     if (rc != ZERO_OK) return rc;
-    if (!valid_dtype(gdtype) || unit < 0 || unit >= plan->n_units) return ZERO_EINVAL;
-    if ((rc = seg_range(plan, unit, begin, count)) != ZERO_OK) return rc;
+    if (!valid_dtype(gdtype) || u0 < 0 || u1 <= u0 || u1 > plan->n_units) return ZERO_EINVAL;
+    begin = plan->unit_seg_begin[u0];
+    count = plan->unit_seg_begin[u1] - begin;
+    if (count > 0x7FFFFFFF) return ZERO_EINVAL;
+    const int64_t f_end = u1 < plan->n_units ? plan->F[u1] : plan->p_pad;
     fill_common(plan, kp);
-    kp.g_origin = plan->F[unit];
-    kp.g_len = plan->S[unit];
+    kp.g_origin = plan->F[u0];
+    kp.g_len = f_end - plan->F[u0];
     kp.seg_base = begin;
-    if (plan->S[unit] == 0) return ZERO_OK;
-    if (grads_unit == nullptr) return ZERO_EINVAL;
+    if (kp.g_len == 0) return ZERO_OK;
+    if (grads_b == nullptr) return ZERO_EINVAL;
     for (int q = 0; q < plan->n_ranks; ++q) {
-        if (grads_unit[q] == nullptr) return ZERO_EINVAL;
-        if (!aligned16(grads_unit[q])) return ZERO_EALIGN;
-        kp.grads[q] = grads_unit[q];
+        if (grads_b[q] == nullptr) return ZERO_EINVAL;
+        if (!aligned16(grads_b[q])) return ZERO_EALIGN;
+        kp.grads[q] = grads_b[q];
     }
     return ZERO_OK;
+}
+
+static int unit_common(const zero_plan *plan, int32_t unit, const void *const *grads_unit, int32_t gdtype,
+                       int64_t &begin, int64_t &count, KParams &kp) {
+    if (plan == nullptr) return ZERO_EINVAL;
+    if (unit < 0 || unit >= plan->n_units) return ZERO_EINVAL;
+    return units_common(plan, unit, unit + 1, grads_unit, gdtype, begin, count, kp);
 }
 
 extern "C" int zero_step_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit, int32_t gdtype,
@@ -330,6 +340,31 @@ extern "C" int zero_step_unit(const zero_plan *plan, int32_t unit, const void *c
     if (rc != ZERO_OK || count == 0) return rc;
     if ((rc = fill_state(plan, kp, master, m, v, pshard, full, pdtype, hp)) != ZERO_OK) return rc;
     return launch_pipe(MODE_FUSED, gdtype, count, kp, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int zero_step_units(const zero_plan *plan, int32_t u0, int32_t u1, const void *const *grads_bucket,
+                               int32_t gdtype, float *const *master, float *const *m, float *const *v, void *full,
+                               void *const *pshard, int32_t pdtype, const zero_hparams *hp, zero_stream_t stream) {
+    if (hp == nullptr || hp->max_norm > 0.0f) return ZERO_EINVAL;  // a global clip needs every unit
+    int64_t begin = 0, count = 0;
+    KParams kp;
+    int rc = units_common(plan, u0, u1, grads_bucket, gdtype, begin, count, kp);
+    if (rc != ZERO_OK || count == 0) return rc;
+    if ((rc = fill_state(plan, kp, master, m, v, pshard, full, pdtype, hp)) != ZERO_OK) return rc;
+    return launch_pipe(MODE_FUSED, gdtype, count, kp, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int zero_clip_reduce_units(const zero_plan *plan, int32_t u0, int32_t u1, const void *const *grads_bucket,
+                                      int32_t gdtype, float *const *gshard, zero_stream_t stream) {
+    int64_t begin = 0, count = 0;
+    KParams kp;
+    int rc = units_common(plan, u0, u1, grads_bucket, gdtype, begin, count, kp);
+    if (rc != ZERO_OK || count == 0) return rc;
+    if ((rc = check_rank_ptrs(plan, reinterpret_cast<const void *const *>(gshard), true)) != ZERO_OK) return rc;
+    kp.write_g = 1;
+    kp.want_partials = 1;
+    for (int q = 0; q < plan->n_ranks; ++q) kp.gshard[q] = gshard[q];
+    return launch_pipe(MODE_REDUCE, gdtype, count, kp, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int zero_reduce_scatter_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit,

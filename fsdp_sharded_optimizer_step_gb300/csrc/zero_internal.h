@@ -25,7 +25,11 @@ static_assert(sizeof(Seg) == 32, "Seg must stay 32 bytes");
 
 // Longest segment.  Segments after the first one of a slice start at a shard
 // position that is a multiple of 8, so 32-byte vector access needs no peeling.
-constexpr int32_t kSegMax = 32768;
+#ifndef ZERO_SEG_MAX
+#define ZERO_SEG_MAX 32768
+#endif
+constexpr int32_t kSegMax = ZERO_SEG_MAX;
+static_assert(kSegMax >= 64 && kSegMax % 8 == 0, "segments hold whole 8-element groups");
 
 // Per-unit description, mirrored into the plan's device workspace.
 struct UnitDesc {

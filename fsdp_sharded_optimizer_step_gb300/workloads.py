@@ -87,6 +87,10 @@ CONFIGS = {
                                "N(0,1e-3); about 3 GB resident",
                           units=lambda: finewrap_units(n_units=128), N=16, gdtype=BF16, pdtype=BF16, stage=2, steps=3,
                           max_norm=0.0, grad_sigma=1e-3, master_sigma=0.02),
+    "4b_z3_prof": dict(desc="profiling case: one 4B block (d=3072, ffn=8192: 113,252,352 params), N=8, ZeRO-3, "
+                            "bf16 grads N(0,1e-3); about 3.6 GB resident",
+                       units=lambda: llm_4b_units()[:1], N=8, gdtype=BF16, pdtype=BF16, stage=3, steps=3,
+                       max_norm=0.0, grad_sigma=1e-3, master_sigma=0.02),
     "4b_z3": dict(desc="4B ZeRO-3: N=8, 33 units, bf16 grads N(0,1e-3), per-unit bf16 all-gather",
                   units=llm_4b_units, N=8, gdtype=BF16, pdtype=BF16, stage=3, steps=3, max_norm=0.0,
                   grad_sigma=1e-3, master_sigma=0.02),

@@ -8,9 +8,9 @@ two units of full weights (Complexity and constants).  "ZeRO: Three Ledgers,
 Zero Redundancy", section 4: gradients streamed through buckets never exist in
 full, which is why stage 1 and stage 2 measure the same.
 
-Orchestration only (streams, events, unit-sized buffers); the gathers and
-reduce-scatters run in the CUDA library (zero_all_gather_unit,
-zero_reduce_scatter_unit).
+Orchestration only (streams, events, unit-sized buffers); the gathers,
+reduce-scatters and updates run in the CUDA library (zero_all_gather_unit,
+zero_reduce_scatter_unit, zero_step_units, zero_clip_reduce_units).
 """
 import torch
 
@@ -95,3 +95,65 @@ class BucketedReduceScatter:
         view = self.bucket[:, :S]
         fill(unit, view)
         B.zero_reduce_scatter_unit(self.plan, unit, view, gshard, coef=coef, stream=stream)
+
+
+def backward_buckets(plan, bucket_elems):
+    """Buckets of consecutive units in backward order (last unit first): each holds
+    units [u0, u1) whose padded sizes add up to at most bucket_elems (a larger unit
+    forms a bucket of its own); units without elements join their neighbours."""
+    out, u = [], plan.n_units
+    while u > 0:
+        u1, total = u, 0
+        while u > 0 and (total == 0 or total + plan.S[u - 1] <= bucket_elems):
+            total += plan.S[u - 1]
+            u -= 1
+        if total > 0:
+            out.append((u, u1))
+    return out
+
+
+class BucketedStep:
+    """The ZeRO-2 step with the gradients streamed through one reusable bucket.
+
+    The backward produces the gradients bucket by bucket, last units first
+    (fill(u0, u1, view) writes the N rank gradients of units [u0, u1) into
+    `view`, on the step's stream); each bucket is consumed as soon as it is full:
+    without clipping by the fused update of its units (zero_step_units: reduce-
+    scatter, AdamW, cast and gather in one launch, no gradient shard in memory);
+    with clipping by its norm pass (zero_clip_reduce_units: averaged fp32
+    gradient shard plus sums of squares), and once every bucket is in, the
+    global coefficient and the shard update.  Same bits as zero_step.  Memory:
+    one bucket of N x bucket_elems gradients instead of N full gradient buffers.
+    bucket_elems: padded elements per bucket (default: the largest unit, at least 2^27)."""
+
+    def __init__(self, plan, grad_dtype=torch.bfloat16, bucket_elems=None):
+        self.plan = plan
+        if bucket_elems is None:
+            bucket_elems = max(max(list(plan.S) + [1]), 1 << 27)
+        self.buckets = backward_buckets(plan, bucket_elems)
+        longest = max([(plan.F[u1] if u1 < plan.n_units else plan.P_pad) - plan.F[u0] for u0, u1 in self.buckets] + [1])
+        self.bucket = B.rank_buffers(plan.n_ranks, longest, grad_dtype, plan.device)
+
+    @property
+    def bucket_bytes(self):
+        return self.bucket.shape[0] * self.bucket.stride(0) * self.bucket.element_size()
+
+    def view(self, u0, u1):
+        end = self.plan.F[u1] if u1 < self.plan.n_units else self.plan.P_pad
+        return self.bucket[:, :end - self.plan.F[u0]]
+
+    def step(self, fill, master, m, v, hp, full=None, pshard=None, gshard=None, sqnorm_out=None, stream=None):
+        clip = hp.max_norm > 0
+        if clip and gshard is None:
+            raise ValueError("a clipped step needs the fp32 gradient shard (gshard)")
+        for u0, u1 in self.buckets:
+            view = self.view(u0, u1)
+            fill(u0, u1, view)
+            if clip:
+                B.zero_clip_reduce_units(self.plan, u0, u1, view, gshard, stream=stream)
+            else:
+                B.zero_step_units(self.plan, u0, u1, view, master, m, v, hp, full=full, pshard=pshard, stream=stream)
+        if clip:
+            B.zero_clip_finalize(self.plan, hp.max_norm, sqnorm_out, stream=stream)
+            B.zero_adamw_shard_step_clipped(self.plan, gshard, master, m, v, hp, pshard=pshard, full=full,
+                                            stream=stream)

@@ -248,6 +248,18 @@ int zero_step_unit(const zero_plan *plan, int32_t unit, const void *const *grads
                    float *const *master, float *const *m, float *const *v, void *full, void *const *pshard,
                    int32_t pdtype, const zero_hparams *hp, zero_stream_t stream);
 
+/* zero_step_unit for the consecutive units [u0, u1) at once, from BUCKET-LOCAL
+ * gradient buffers: grads_bucket[q] (DEVICE, 16-byte aligned) holds rank q's
+ * padded gradient positions of those units, element i = full position F_u0 + i
+ * (F_u1 - F_u0 elements).  A bucket of several units is one launch; this is
+ * ZeRO-2's gradient bucket ("ZeRO: Three Ledgers, Zero Redundancy", section 4:
+ * gradients streamed through buckets and reduced as they fill, so the N full
+ * gradient buffers never exist).  0 <= u0 < u1 <= n_units.  No clipping.
+ * Results equal zero_step's bit for bit.  Errors: as zero_step_unit. */
+int zero_step_units(const zero_plan *plan, int32_t u0, int32_t u1, const void *const *grads_bucket, int32_t gdtype,
+                    float *const *master, float *const *m, float *const *v, void *full, void *const *pshard,
+                    int32_t pdtype, const zero_hparams *hp, zero_stream_t stream);
+
 /* zero_reduce_scatter for unit `unit` only, from unit-local gradient buffers
  * (as zero_step_unit): gshard[r][Hoff_u + j] for the unit's slices. */
 int zero_reduce_scatter_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit, int32_t gdtype,
@@ -258,7 +270,8 @@ int zero_reduce_scatter_unit(const zero_plan *plan, int32_t unit, const void *co
  * notes; a norm is a decomposable sum of squares, "ZeRO: Three Ledgers, Zero
  * Redundancy", section 2).  Three calls, in this order on one stream:
  *
- * 1. zero_clip_reduce_unit for every unit with S_u > 0, in any order, each
+ * 1. zero_clip_reduce_unit for every unit with S_u > 0 (or zero_clip_reduce_units
+ *    for buckets of consecutive units), in any order, each
  *    from unit-local gradient buffers (as zero_step_unit): writes the unit's
  *    averaged fp32 gradient into gshard[r][Hoff_u + j] and the sums of squares
  *    of the unit's launch-table segments into the plan's workspace.
@@ -275,6 +288,10 @@ int zero_reduce_scatter_unit(const zero_plan *plan, int32_t unit, const void *co
  * returns ZERO_EINVAL for max_norm <= 0. */
 int zero_clip_reduce_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit, int32_t gdtype,
                           float *const *gshard, zero_stream_t stream);
+/* Step 1 for the consecutive units [u0, u1) at once, from a bucket-local
+ * gradient buffer laid out as for zero_step_units. */
+int zero_clip_reduce_units(const zero_plan *plan, int32_t u0, int32_t u1, const void *const *grads_bucket,
+                           int32_t gdtype, float *const *gshard, zero_stream_t stream);
 int zero_clip_finalize(const zero_plan *plan, float max_norm, double *sqnorm_dev, zero_stream_t stream);
 int zero_adamw_shard_step_clipped(const zero_plan *plan, const float *const *gshard, float *const *master,
                                   float *const *m, float *const *v, void *const *pshard, void *full, int32_t pdtype,

@@ -593,6 +593,41 @@ def test_zero2_bucketed_reduce_scatter_then_shard_update_equals_fused_step():
         assert torch.equal(host_bits_t(x), host_bits_t(y))
 
 
+@pytest.mark.parametrize("bucket_elems,max_norm", [(1, 0.0), (150000, 0.0), (None, 0.0), (150000, 1e-3), (1, 1e6)])
+def test_zero2_bucketed_step_bit_exact(bucket_elems, max_norm):
+    """The ZeRO-2 step through one reusable gradient bucket, filled in backward order:
+    one unit per bucket, several units per bucket, everything in one bucket; with
+    clipping the buckets' norm passes, then the coefficient and the shard update.
+    Every step equals the oracle's, S included."""
+    from fsdp_sharded_optimizer_step_gb300.zero3 import BucketedStep
+    sizes = W.finewrap_units(n_units=25, lo_log2=2, hi_log2=16, seed=12) + [70001, 0, 3]
+    c = SmallCase(sizes, 8, W.BF16, W.BF16, seed=14, grad_sigma=1e-2, outlier_frac=1e-3, outlier_scale=100.0)
+    bs = BucketedStep(c.plan, bucket_elems=bucket_elems)
+    assert bs.bucket_bytes < c.grads.shape[0] * c.grads.stride(0) * 2 or bucket_elems is None
+    if bucket_elems == 1:
+        assert len(bs.buckets) == sum(1 for s in c.plan.S if s)
+    seen = []
+
+    def fill(u0, u1, view):  # stands in for the backward of units [u0, u1)
+        seen.append((u0, u1))
+        F0 = c.plan.F[u0]
+        view.copy_(c.grads[:, F0:F0 + view.shape[1]])
+
+    for t in (1, 2):
+        hp, _ = hp_for(t, max_norm)
+        bs.step(fill, c.master, c.m, c.v, hp, full=c.full, pshard=c.pshard, gshard=c.gshard, sqnorm_out=c.sq)
+        torch.cuda.synchronize()
+        assert c.oracle_step(t, max_norm=max_norm) == O.OK
+        if max_norm > 0:
+            assert abs(c.sq.item() - c.S_o) <= S_RTOL * c.S_o
+            assert O.clip_coef(c.sq.item(), max_norm) == O.clip_coef(c.S_o, max_norm)
+        c.assert_state_equal()
+        c.assert_full_equal()
+        c.assert_pshard_equal()
+    covered = sorted(u for u0, u1 in seen[:len(bs.buckets)] for u in range(u0, u1))
+    assert covered == [u for u in range(len(sizes)) if c.plan.S[u] or u in covered]
+
+
 # ------------------------------------------------------------------ failure detection without a GPU fault
 def test_bounded_wait_runs_out_and_is_reported():
     """A pipeline stage that never fills (one tile's copies dropped in the first segment by the
