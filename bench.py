@@ -150,7 +150,9 @@ class ClockSampler:
         mx = [num(p[2]) for p in use if num(p[2]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for p in use for i in range(4) if p[5 + i].lower().startswith("active")})
+        pw = [num(p[3]) for p in use if num(p[3]) is not None]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "sm_mhz_min": min(sm) if sm else None, "power_w_max": max(pw) if pw else None,
                 "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside)}
 
 
@@ -722,16 +724,22 @@ def eng_batches(plan, batch_min):
     return out
 
 
-def _time_ms(fn, stream, reps):
-    fn()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(reps):
+def _time_ms(fn, stream, reps, rounds=3, warm=2):
+    """Mean ms per call of fn over reps back-to-back calls (CUDA events on `stream`),
+    after `warm` untimed calls; the best of `rounds` such runs."""
+    for _ in range(warm):
         fn()
-    e1.record(stream)
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / reps
+    best = float("inf")
+    for _ in range(rounds):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1) / reps)
+    return best
 
 
 def run_unit_flows(args, world, rank, local):
@@ -750,8 +758,11 @@ def run_unit_flows(args, world, rank, local):
     P, H = plan.P_pad, plan.H
     stream = torch.cuda.current_stream(dev)
     reps = max(args.steps, 1)
-    out = {"n_gpus": world, "steps": reps, "warmup": 1, "data": "synthetic",
+    out = {"n_gpus": world, "steps": reps, "warmup": 2, "data": "synthetic",
            "config": {"workload": f"{args.config}: {cfg['desc']}", "units": len(sizes)}}
+    clocks = ClockSampler(local)
+    clocks.start()
+    clocks.begin()
     if args.op == "zero3_gather":
         pshard = Z.rank_buffers(N, H, torch.bfloat16, dev)
         pshard.normal_()
@@ -811,13 +822,16 @@ def run_unit_flows(args, world, rank, local):
         t_rs = _time_ms(lambda: [Z.zero_reduce_scatter_unit(plan, u, buckets.bucket[:, :plan.S[u]], gshard)
                                  for u in reversed(range(plan.n_units))], stream, reps)
         t_shard = _time_ms(lambda: Z.zero_adamw_shard_step(plan, gshard, master, m, v, hp, full=full), stream, reps)
+        t_fused_end = _time_ms(lambda: Z.zero_step(plan, grads, master, m, v, hp, full=full), stream, reps)
         best = flows["default buckets"]["bucket_updates_ms"]
         out.update(metric="ZeRO-2 bucketed step: bucket updates of the default bucketing (ms per step)",
                    value=best, unit="ms", higher_is_better=False,
-                   flow={"fused_step_ms": t_fused, "bucketed": flows,
+                   flow={"fused_step_ms": t_fused, "fused_step_ms_at_the_end": t_fused_end, "bucketed": flows,
                          "vs_fused": best / t_fused,
                          "shard_route_ms": {"reduce_scatter_per_unit": t_rs, "shard_update": t_shard},
                          "full_gradient_bytes": N * P * 2, "gradient_shard_bytes": N * H * 4})
+    clocks.end()
+    out["clocks"] = clocks.stop()
     if rank == 0:
         print(json.dumps(out), flush=True)
     return 0

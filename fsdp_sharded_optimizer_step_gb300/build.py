@@ -23,7 +23,7 @@ CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-ffp-contract=off", "-fno-fast-math"
 
 SOURCES_CU = ["zero_kernels.cu", "zero_abi.cu", "zero_noalloc.cu", "zero_reshard.cu"]
 SOURCES_CXX = ["zero_plan.cpp", "zero_offload.cpp"]
-HEADERS = ["zero_internal.h", "zero_launch.h"]
+HEADERS = ["zero_internal.h", "zero_launch.h", "zero_nvtx.h"]
 # the host update of the offloaded step: vectorised (-O3; -fno-math-errno lets sqrt
 # become one instruction), still one rounding per operation (-ffp-contract=off)
 CXX_EXTRA = {"zero_offload.cpp": ["-O3", "-fno-math-errno", "-pthread"]}
@@ -81,7 +81,7 @@ def _build_into(out_dir, defines, force, verbose):
     if failed:
         raise RuntimeError("building the CUDA library failed (see compiler output above)")
     tmp = lib + f".tmp{os.getpid()}"
-    subprocess.run([NVCC, *ARCH, "-shared", "-Xcompiler", "-fPIC", *objs, "-o", tmp, "-lpthread"], check=True)
+    subprocess.run([NVCC, *ARCH, "-shared", "-Xcompiler", "-fPIC", *objs, "-o", tmp, "-lpthread", "-ldl"], check=True)
     os.replace(tmp, lib)
     return lib
 

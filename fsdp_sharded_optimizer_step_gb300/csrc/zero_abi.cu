@@ -6,6 +6,7 @@
 #include <cstdint>
 
 #include "zero_launch.h"
+#include "zero_nvtx.h"
 
 namespace zero {
 
@@ -100,6 +101,7 @@ using namespace zero;
 
 // ------------------------------------------------------------------ C ABI
 extern "C" int zero_plan_attach(zero_plan *plan, void *workspace, size_t bytes, zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     if (plan == nullptr || workspace == nullptr || plan->attached) return ZERO_EINVAL;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ZERO_EALIGN;
     const WsLayout L = workspace_layout(plan);
@@ -114,12 +116,14 @@ extern "C" int zero_plan_attach(zero_plan *plan, void *workspace, size_t bytes, 
         if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
     }
     plan->d_segs = reinterpret_cast<Seg *>(base + L.segs);
-    plan->d_partials = reinterpret_cast<double *>(base + L.partials);
+    plan->d_partials = reinterpret_cast<SqPartial *>(base + L.partials);
     plan->d_sqnorm = reinterpret_cast<double *>(base + L.scalars);
     plan->d_coef = reinterpret_cast<float *>(base + L.scalars + 8);
     plan->d_err = reinterpret_cast<int *>(base + L.scalars + 16);
     plan->d_tickets = reinterpret_cast<unsigned long long *>(base + L.scalars + 24);
     plan->d_skipped = reinterpret_cast<int *>(base + L.scalars + 40);
+    plan->d_fin_count = reinterpret_cast<unsigned *>(base + L.scalars + 48);
+    plan->d_fin_sums = reinterpret_cast<double *>(base + L.fin);
     if (!plan->unit_table.empty()) {
         e = cudaMemcpyAsync(base + L.units, plan->unit_table.data(), plan->unit_table.size() * sizeof(UnitDesc),
                             cudaMemcpyHostToDevice, reinterpret_cast<cudaStream_t>(stream));
@@ -135,6 +139,7 @@ extern "C" int zero_plan_attach(zero_plan *plan, void *workspace, size_t bytes, 
 
 extern "C" int zero_reduce_scatter(const zero_plan *plan, const void *const *grads, int32_t gdtype,
                                    float *const *gshard, float coef, zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     int rc = check_attached(plan);
     if (rc != ZERO_OK) return rc;
     if (!valid_dtype(gdtype)) return ZERO_EINVAL;
@@ -168,12 +173,12 @@ static int launch_norm(const zero_plan *plan, const void *const *grads, int32_t 
     const int64_t nseg = static_cast<int64_t>(plan->segs.size());
     const int rc = launch_pipe(MODE_REDUCE, gdtype, nseg, kp, st);
     if (rc != ZERO_OK) return rc;
-    return launch_finalize(plan->d_partials, nseg, max_norm, plan->d_sqnorm, sqnorm_out, plan->d_coef,
-                           plan->d_skipped, st);
+    return launch_finalize(plan, max_norm, sqnorm_out, st);
 }
 
 extern "C" int zero_grad_sqnorm(const zero_plan *plan, const void *const *grads, int32_t gdtype, double *sqnorm_dev,
                                 zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     int rc = check_attached(plan);
     if (rc != ZERO_OK) return rc;
     if (!valid_dtype(gdtype) || sqnorm_dev == nullptr) return ZERO_EINVAL;
@@ -207,6 +212,7 @@ static int fill_state(const zero_plan *plan, KParams &kp, float *const *master, 
 extern "C" int zero_adamw_shard_step(const zero_plan *plan, const float *const *gshard, float *const *master,
                                      float *const *m, float *const *v, void *const *pshard, void *full, int32_t pdtype,
                                      const zero_hparams *hp, zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     int rc = check_attached(plan);
     if (rc != ZERO_OK) return rc;
     if ((rc = check_rank_ptrs(plan, reinterpret_cast<const void *const *>(gshard), true)) != ZERO_OK) return rc;
@@ -220,6 +226,7 @@ extern "C" int zero_adamw_shard_step(const zero_plan *plan, const float *const *
 
 extern "C" int zero_all_gather(const zero_plan *plan, const void *const *shard, void *full, int32_t pdtype, int32_t unit,
                                zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     int rc = check_attached(plan);
     if (rc != ZERO_OK) return rc;
     if (!valid_dtype(pdtype)) return ZERO_EINVAL;
@@ -239,6 +246,7 @@ extern "C" int zero_all_gather(const zero_plan *plan, const void *const *shard, 
 
 extern "C" int zero_all_gather_unit(const zero_plan *plan, int32_t unit, const void *const *shard, void *dst_unit,
                                     int32_t pdtype, zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     int rc = check_attached(plan);
     if (rc != ZERO_OK) return rc;
     if (!valid_dtype(pdtype) || unit < 0 || unit >= plan->n_units) return ZERO_EINVAL;
@@ -260,6 +268,7 @@ extern "C" int zero_all_gather_unit(const zero_plan *plan, int32_t unit, const v
 
 extern "C" int zero_all_gather_bf16(const zero_plan *plan, const uint16_t *const *shard16, uint16_t *full, int32_t unit,
                                     zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     return zero_all_gather(plan, reinterpret_cast<const void *const *>(shard16), full, ZERO_BF16, unit, stream);
 }
 
@@ -267,6 +276,7 @@ extern "C" int zero_step(const zero_plan *plan, const void *const *grads, int32_
                          float *const *m, float *const *v, void *full, void *const *pshard, int32_t pdtype,
                          float *const *gshard_ws, const zero_hparams *hp, double *sqnorm_dev, int32_t unit,
                          zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     int rc = check_attached(plan);
     if (rc != ZERO_OK) return rc;
     if (!valid_dtype(gdtype) || hp == nullptr) return ZERO_EINVAL;
@@ -333,6 +343,7 @@ static int unit_common(const zero_plan *plan, int32_t unit, const void *const *g
 extern "C" int zero_step_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit, int32_t gdtype,
                               float *const *master, float *const *m, float *const *v, void *full, void *const *pshard,
                               int32_t pdtype, const zero_hparams *hp, zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     if (hp == nullptr || hp->max_norm > 0.0f) return ZERO_EINVAL;  // a global clip needs every unit
     int64_t begin = 0, count = 0;
     KParams kp;
@@ -345,6 +356,7 @@ extern "C" int zero_step_unit(const zero_plan *plan, int32_t unit, const void *c
 extern "C" int zero_step_units(const zero_plan *plan, int32_t u0, int32_t u1, const void *const *grads_bucket,
                                int32_t gdtype, float *const *master, float *const *m, float *const *v, void *full,
                                void *const *pshard, int32_t pdtype, const zero_hparams *hp, zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     if (hp == nullptr || hp->max_norm > 0.0f) return ZERO_EINVAL;  // a global clip needs every unit
     int64_t begin = 0, count = 0;
     KParams kp;
@@ -356,6 +368,7 @@ extern "C" int zero_step_units(const zero_plan *plan, int32_t u0, int32_t u1, co
 
 extern "C" int zero_clip_reduce_units(const zero_plan *plan, int32_t u0, int32_t u1, const void *const *grads_bucket,
                                       int32_t gdtype, float *const *gshard, zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     int64_t begin = 0, count = 0;
     KParams kp;
     int rc = units_common(plan, u0, u1, grads_bucket, gdtype, begin, count, kp);
@@ -369,6 +382,7 @@ extern "C" int zero_clip_reduce_units(const zero_plan *plan, int32_t u0, int32_t
 
 extern "C" int zero_reduce_scatter_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit,
                                         int32_t gdtype, float *const *gshard, float coef, zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     int64_t begin = 0, count = 0;
     KParams kp;
     int rc = unit_common(plan, unit, grads_unit, gdtype, begin, count, kp);
@@ -382,6 +396,7 @@ extern "C" int zero_reduce_scatter_unit(const zero_plan *plan, int32_t unit, con
 
 extern "C" int zero_clip_reduce_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit,
                                      int32_t gdtype, float *const *gshard, zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     int64_t begin = 0, count = 0;
     KParams kp;
     int rc = unit_common(plan, unit, grads_unit, gdtype, begin, count, kp);
@@ -394,18 +409,19 @@ extern "C" int zero_clip_reduce_unit(const zero_plan *plan, int32_t unit, const 
 }
 
 extern "C" int zero_clip_finalize(const zero_plan *plan, float max_norm, double *sqnorm_dev, zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     int rc = check_attached(plan);
     if (rc != ZERO_OK) return rc;
     if (!(max_norm > 0.0f)) return ZERO_EINVAL;
     if (sqnorm_dev != nullptr && (reinterpret_cast<uintptr_t>(sqnorm_dev) & 7u) != 0) return ZERO_EALIGN;
-    return launch_finalize(plan->d_partials, static_cast<int64_t>(plan->segs.size()), max_norm, plan->d_sqnorm,
-                           sqnorm_dev, plan->d_coef, plan->d_skipped, reinterpret_cast<cudaStream_t>(stream));
+    return launch_finalize(plan, max_norm, sqnorm_dev, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int zero_adamw_shard_step_clipped(const zero_plan *plan, const float *const *gshard, float *const *master,
                                              float *const *m, float *const *v, void *const *pshard, void *full,
                                              int32_t pdtype, const zero_hparams *hp, int32_t unit,
                                              zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     int rc = check_attached(plan);
     if (rc != ZERO_OK) return rc;
     if ((rc = check_rank_ptrs(plan, reinterpret_cast<const void *const *>(gshard), true)) != ZERO_OK) return rc;
@@ -428,6 +444,7 @@ extern "C" int zero_debug_drop_copy(int64_t tile) {
 }
 
 extern "C" int zero_plan_check(const zero_plan *plan, zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     int rc = check_attached(plan);
     if (rc != ZERO_OK) return rc;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

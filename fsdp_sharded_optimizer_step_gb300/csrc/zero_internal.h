@@ -16,20 +16,43 @@ namespace zero {
 struct Seg {
     int64_t g_off;  // full-buffer position of the segment's first element: F_u + r*h_u + j0
     int64_t s_off;  // shard-buffer position of the same element: Hoff_u + j0
-    int32_t len;    // elements in the segment (1..kSegMax)
+    int32_t len;    // elements in the segment (1..seg_max_for(N))
     int32_t valid;  // elements before the unit's padding starts (0..len)
     int32_t rank;
     int32_t unit;
 };
 static_assert(sizeof(Seg) == 32, "Seg must stay 32 bytes");
 
-// Longest segment.  Segments after the first one of a slice start at a shard
-// position that is a multiple of 8, so 32-byte vector access needs no peeling.
-#ifndef ZERO_SEG_MAX
-#define ZERO_SEG_MAX 32768
+// Longest segment: 8192 elements for up to 8 ranks, 32768 for more (measured:
+// at N = 8 the shorter segments shorten the tail of every launch, which per-unit
+// and per-bucket launches pay each time; at N = 16 the pipeline's 1536-element
+// tile fits the longer segment better).  ZERO_SEG_MAX fixes one length for all
+// N (for measurements).  Segments after the first one of a slice start at a
+// shard position that is a multiple of 8, so 32-byte vector access needs no
+// peeling.
+constexpr int32_t kSegMaxSmallN = 8192, kSegMaxLargeN = 32768;
+inline int32_t seg_max_for(int32_t n_ranks) {
+#ifdef ZERO_SEG_MAX
+    (void)n_ranks;
+    static_assert(ZERO_SEG_MAX >= 64 && ZERO_SEG_MAX % 8 == 0 && ZERO_SEG_MAX <= kSegMaxLargeN,
+                  "segments hold whole 8-element groups");
+    return ZERO_SEG_MAX;
+#else
+    return n_ranks <= 8 ? kSegMaxSmallN : kSegMaxLargeN;
 #endif
-constexpr int32_t kSegMax = ZERO_SEG_MAX;
-static_assert(kSegMax >= 64 && kSegMax % 8 == 0, "segments hold whole 8-element groups");
+}
+
+// Per segment, the clip's sum of squares is kept as kPartialSlots partials
+// (one per consumer warp of the pipelined kernel; unused slots hold 0), added
+// later in a fixed order.  A partial is a binary32 pair (hi + lo, the warp's
+// squares added in pair arithmetic) plus a binary64 part for values outside the
+// pair's range; the binary64 work happens only when the partials are added up.
+struct SqPartial {
+    float hi, lo;
+    double wide;
+};
+static_assert(sizeof(SqPartial) == 16, "SqPartial must stay 16 bytes");
+constexpr int kPartialSlots = 16;
 
 // Per-unit description, mirrored into the plan's device workspace.
 struct UnitDesc {
@@ -65,19 +88,24 @@ struct zero_plan {
     bool attached = false;
     int device = -1;
     zero::Seg *d_segs = nullptr;
-    double *d_partials = nullptr;   // one binary64 partial sum per segment
+    zero::SqPartial *d_partials = nullptr;  // kPartialSlots partial sums of squares per segment
     double *d_sqnorm = nullptr;     // S of the last clipped step
     float *d_coef = nullptr;        // clip coefficient of the last clipped step
     int *d_err = nullptr;           // device error word: non-zero after a bounded wait expired
     unsigned long long *d_tickets = nullptr;  // [2]: segment tickets and finished CTAs of a pipelined launch
     int *d_skipped = nullptr;       // non-zero after a clipped step found a non-finite norm (zero_plan_check)
+    unsigned *d_fin_count = nullptr;  // blocks of the total's first pass done (0 between launches)
+    double *d_fin_sums = nullptr;   // kFinBlocks per-block sums of the total's first pass
     zero::UnitDesc *d_units = nullptr;  // device unit table
 };
 
 namespace zero {
+// Blocks of the fixed-order total of the partials (its first pass).
+constexpr int kFinBlocks = 128;
+
 // Workspace layout (byte offsets from the workspace base).
 struct WsLayout {
-    size_t segs, partials, scalars, units, total;
+    size_t segs, partials, scalars, units, fin, total;
 };
 WsLayout workspace_layout(const zero_plan *plan);
 int adam_consts(const zero_hparams *hp, AdamConsts *out);

@@ -5,8 +5,8 @@
 // cores): per padded element the fused step reads N gradients plus master/m/v
 // and writes master/m/v plus the gathered param.  k_pipe is a persistent,
 // warp-specialised kernel: per CTA one producer thread streams segment tiles
-// into a shared-memory ring with bulk copies while 16 consumer warps compute
-// from the ring, and segments are handed out dynamically from a ticket
+// into a shared-memory ring with bulk copies while 12 or 16 consumer warps
+// compute from the ring, and segments are handed out dynamically from a ticket
 // counter.  k_finalize adds the clip's per-segment partial sums in a fixed
 // order; k_gather is the per-unit all-gather.
 //
@@ -24,12 +24,22 @@
 namespace zero {
 
 constexpr int kThreads = 256;
-#ifndef ZERO_PIPE_CONSUMER_WARPS
-#define ZERO_PIPE_CONSUMER_WARPS 16
-#endif
-constexpr int kConsumerWarps = ZERO_PIPE_CONSUMER_WARPS;
-constexpr int kPipeThreads = (kConsumerWarps + 1) * 32;
 constexpr int kSegRing = 8;  // segment numbers the producer may take ahead of its consumers
+
+// Consumer warps of k_pipe for NR gradient rows (0: any count): 16, or 12 for
+// 16 rows, where a stage holds a 1536-element tile (two stages fit the shared
+// memory budget) and 12 warps take it in exactly one pass of 4 elements per
+// thread.  ZERO_PIPE_CONSUMER_WARPS overrides the choice (for measurements).
+template <int NR>
+__host__ __device__ constexpr int consumer_warps() {
+#ifdef ZERO_PIPE_CONSUMER_WARPS
+    return ZERO_PIPE_CONSUMER_WARPS;
+#else
+    return NR >= 16 ? 12 : 16;
+#endif
+}
+static_assert(consumer_warps<16>() <= kPartialSlots && consumer_warps<8>() <= kPartialSlots,
+              "one partial slot per consumer warp");
 
 // Diagnostic build (-DZERO_SELFCHECK): every shared/global access of the
 // pipeline is checked against its buffer and alignment first; a failed check
@@ -241,13 +251,14 @@ __device__ __forceinline__ SegSplit split_segment(const Seg &sg, int64_t g_origi
 // square is split exactly into a binary32 pair (hi = fl(g*g), lo = fma(g, g,
 // -hi), an error-free product), the pairs are added with TwoSum into a
 // binary32 (hi, lo) accumulator that is renormalised after every add, and
-// the accumulator is widened to binary64 once per segment.  The pair is
-// error-free only while every bit of g*g is representable: |g| >= 2^-51 keeps
-// the lowest bit of g*g at or above 2^-148 (the error term is never a
-// rounded subnormal), and |g| <= 2^60 keeps 64 squares below 2^128.  Values
-// outside that range (and inf/NaN) go to a binary64 accumulator directly.
-// Relative error per segment and thread is below ~1e-13 for the <= 64
-// squares a thread adds there.
+// the warps' accumulators are added across the warp in the same pair
+// arithmetic at the end of a segment; the pair goes to binary64 only when the
+// partials are added up (k_finalize).  The pair is error-free only while every
+// bit of g*g is representable: |g| >= 2^-51 keeps the lowest bit of g*g at or
+// above 2^-148 (the error term is never a rounded subnormal), and |g| <= 2^56
+// keeps the squares one warp adds in a segment (at most 32 x 86) below 2^125.
+// Values outside that range (and inf/NaN) go to a binary64 accumulator
+// directly.  Relative error per segment and warp is below ~1e-13.
 struct SqAcc {
     float hi, lo;
     double wide;
@@ -261,7 +272,7 @@ __device__ __forceinline__ void sq_reset(SqAcc &a) {
 
 __device__ __forceinline__ void add_square(SqAcc &a, float g) {
     const float mag = fabsf(g);
-    if (!(mag <= 0x1p60f) || (mag < 0x1p-51f && mag != 0.0f)) {
+    if (!(mag <= 0x1p56f) || (mag < 0x1p-51f && mag != 0.0f)) {
         const double d = static_cast<double>(g);
         a.wide = __dadd_rn(a.wide, __dmul_rn(d, d));
         return;
@@ -276,8 +287,33 @@ __device__ __forceinline__ void add_square(SqAcc &a, float g) {
     a.lo = __fsub_rn(l, __fsub_rn(a.hi, t));
 }
 
-__device__ __forceinline__ double sq_total(const SqAcc &a) {
-    return __dadd_rn(__dadd_rn(static_cast<double>(a.hi), static_cast<double>(a.lo)), a.wide);
+// (hi, lo) += (bhi, blo) in binary32 pair arithmetic: TwoSum of the high parts,
+// the low parts and the error added, then renormalised (FastTwoSum).
+__device__ __forceinline__ void pair_add(float &hi, float &lo, float bhi, float blo) {
+    const float s = __fadd_rn(hi, bhi);
+    const float bp = __fsub_rn(s, hi);
+    const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(bhi, bp));
+    const float t = __fadd_rn(__fadd_rn(lo, blo), e);
+    hi = __fadd_rn(s, t);
+    lo = __fsub_rn(t, __fsub_rn(hi, s));
+}
+
+// A warp's accumulators added across the warp (a fixed shuffle tree; lane 0
+// holds the result): the pair in binary32 pair arithmetic, the binary64 part only
+// when some lane has one (values outside the pair's range are rare).
+__device__ __forceinline__ SqPartial warp_sq(const SqAcc &a) {
+    SqPartial r{a.hi, a.lo, a.wide};
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ohi = __shfl_down_sync(0xFFFFFFFFu, r.hi, o);
+        const float olo = __shfl_down_sync(0xFFFFFFFFu, r.lo, o);
+        pair_add(r.hi, r.lo, ohi, olo);
+    }
+    if (__any_sync(0xFFFFFFFFu, __double_as_longlong(r.wide) != 0)) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) r.wide = __dadd_rn(r.wide, __shfl_down_sync(0xFFFFFFFFu, r.wide, o));
+    }
+    return r;
 }
 
 // Direct (register) path for one segment, spread over nthr threads: the
@@ -530,7 +566,7 @@ __device__ __forceinline__ void consume_tile(const KParams &p, const Seg &sg, co
                                              bool scale, float coef, SqAcc &sq, float *__restrict__ Wg,
                                              float *__restrict__ Mg, float *__restrict__ Vg, float *__restrict__ Gg,
                                              void *full, void *ps, int n) {
-    constexpr int CT = kConsumerWarps * 32;
+    constexpr int CT = consumer_warps<NR>() * 32;
     const float *Ws = reinterpret_cast<const float *>(buf + L.state_off);
     const float *Ms = Ws + tile;
     const float *Vs = Ms + tile;
@@ -595,7 +631,8 @@ __device__ __forceinline__ bool pipe_eligible(const KParams &p, const Seg &sg, c
 }
 
 template <int MODE, int GD, int NR>
-__global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64_t nseg) {
+__global__ void __launch_bounds__((consumer_warps<NR>() + 1) * 32, 1) k_pipe(const KParams p, int64_t nseg) {
+    constexpr int CW = consumer_warps<NR>();
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int GB = GD == ZERO_BF16 ? 2 : 4;  // bytes per gradient element
     constexpr int SHIFT_MASK = 16 / GB - 1;      // elements per 16 bytes, minus one
@@ -615,28 +652,25 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64
     __shared__ int abort_flag;
     // segment ring: the producer publishes each segment number it took (-1: no more) in
     // seg_ring[slot] and arrives on seg_full[slot]; every consumer warp arrives on
-    // seg_empty[slot] once done with the number (warp 0 only after the segment's sum of
-    // squares, which it adds up from red_smem[slot] once red_full[slot] completes)
+    // seg_empty[slot] once it has read the number
     __shared__ int64_t seg_ring[kSegRing];
-    __shared__ __align__(8) uint64_t seg_full[kSegRing], seg_empty[kSegRing], red_full[kSegRing];
-    __shared__ double red_smem[kSegRing][kConsumerWarps];
+    __shared__ __align__(8) uint64_t seg_full[kSegRing], seg_empty[kSegRing];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], kConsumerWarps);
+            mbar_init(&empty_bar[s], CW);
         }
         for (int s = 0; s < kSegRing; ++s) {
             mbar_init(&seg_full[s], 1);
-            mbar_init(&seg_empty[s], kConsumerWarps);
-            mbar_init(&red_full[s], kConsumerWarps);
+            mbar_init(&seg_empty[s], CW);
         }
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
 
-    if (warp == kConsumerWarps) {
+    if (warp == CW) {
         // ---------------- producer
         if (lane != 0) return;
         int stage = 0;
@@ -743,8 +777,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64
     // (a stage shared between consumer sets that alternate would let a waiter
     // for phase k pass while the barrier is still in phase k-1: the parity of
     // phase k then reads as already complete).
-    const int ct = threadIdx.x;  // 0 .. kConsumerWarps*32 - 1
-    constexpr int CT = kConsumerWarps * 32;
+    const int ct = threadIdx.x;  // 0 .. CW*32 - 1
+    constexpr int CT = CW * 32;
     int stage = 0;
     uint32_t phase = 0;
     bool dead = false;  // a stage wait gave up: stop consuming tiles, keep taking part in the rings
@@ -759,14 +793,12 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64
         }
         const int64_t si = *reinterpret_cast<volatile int64_t *>(&seg_ring[rs]);
         const int slot = rs;
-        const uint32_t slot_phase = rphase;
         if (++rs == kSegRing) {
             rs = 0;
             rphase ^= 1u;
         }
-        const bool reduce_here = MODE == MODE_REDUCE && p.want_partials && si >= 0;
         __syncwarp();
-        if (lane == 0 && !(reduce_here && warp == 0)) mbar_arrive(&seg_empty[slot]);
+        if (lane == 0) mbar_arrive(&seg_empty[slot]);
         if (si < 0) break;
         const Seg sg = p.segs[p.seg_base + si];
         const SegSplit sp = split_segment(sg, p.g_origin);
@@ -810,30 +842,14 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_pipe(const KParams p, int64
             }
         }
         if constexpr (MODE == MODE_REDUCE) {
-            if (p.want_partials) {  // the segment's sum of squares, in a fixed order
-                double x = sq_total(sq);
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) x = __dadd_rn(x, __shfl_down_sync(0xFFFFFFFFu, x, o));
+            if (p.want_partials) {
+                // this warp's share of the segment's sum of squares, in the warp's own slot: no
+                // warp waits for another; the slots past the consumer warps are written as 0
+                const SqPartial x = warp_sq(sq);
                 if (lane == 0) {
-                    red_smem[slot][warp] = x;
-                    mbar_arrive(&red_full[slot]);  // release: warp 0 sees x once the phase completes
-                }
-                if (warp == 0) {
-                    // warp 0 hands the slot back (seg_empty) only after this read, so no warp can
-                    // write a later segment's value into red_smem[slot] before it
-                    if (__all_sync(0xFFFFFFFFu, mbar_wait(&red_full[slot], slot_phase))) {
-                        double t = lane < kConsumerWarps
-                                       ? *reinterpret_cast<volatile double *>(&red_smem[slot][lane])
-                                       : 0.0;
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) t = __dadd_rn(t, __shfl_down_sync(0xFFFFFFFFu, t, o));
-                        if (lane == 0) p.partials[p.seg_base + si] = t;
-                    } else {
-                        if (lane == 0) atomicExch(p.err, 4);
-                        abort_flag = 1;
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&seg_empty[slot]);
+                    SqPartial *dst = p.partials + (p.seg_base + si) * kPartialSlots;
+                    dst[warp] = x;
+                    if (warp < kPartialSlots - CW) dst[CW + warp] = SqPartial{0.0f, 0.0f, 0.0};
                 }
             }
         }
@@ -856,19 +872,45 @@ __device__ __forceinline__ double block_sum(double x, double *smem) {
     return s;  // valid in thread 0
 }
 
-// One CTA adds the per-segment partials in a fixed order (thread t takes
-// segments t, t+1024, ... in sequence, then a fixed tree), writes S and, when
-// max_norm > 0, the clip coefficient min(1, max_norm / (sqrt(S) + 1e-6))
-// rounded once to binary32 (NaN when S is not finite: the update then skips).
-constexpr int kFinThreads = 1024;
-__global__ void __launch_bounds__(kFinThreads) k_finalize(const double *partials, int64_t nseg, float max_norm,
+// The fixed-order total of the segments' partials (kPartialSlots each, each
+// widened to binary64 as (hi + lo) + wide), in one
+// launch of kFinBlocks-or-fewer CTAs.  CTA b adds the contiguous block b of the
+// partials (thread t takes partials t, t + kFinThreads, ... of the block in
+// sequence, then a fixed tree) and stores its sum; the CTA that finishes last
+// (a counter, no waiting) adds the block sums in block order with the same
+// tree, writes S and, when max_norm > 0, the clip coefficient
+// min(1, max_norm / (sqrt(S) + 1e-6)) rounded once to binary32 (NaN when S is
+// not finite: the update then skips), and resets the counter for the next
+// launch.  The blocks depend only on the number of partials, so S is the same
+// bits on every run and every GPU.
+constexpr int kFinThreads = 512;
+__global__ void __launch_bounds__(kFinThreads) k_finalize(const SqPartial *partials, int64_t n, int64_t block,
+                                                          float max_norm, double *block_sums, unsigned *done,
                                                           double *sqnorm_ws, double *sqnorm_out, float *coef_out,
                                                           int *skipped) {
     __shared__ double smem[kFinThreads / 32];
+    __shared__ bool last;
+    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * block;
+    const int64_t b1 = b0 + block < n ? b0 + block : n;
     double s = 0.0;
-    for (int64_t i = threadIdx.x; i < nseg; i += kFinThreads) s = __dadd_rn(s, partials[i]);
-    const double S = block_sum(s, smem);
+    for (int64_t i = b0 + threadIdx.x; i < b1; i += kFinThreads) {
+        const SqPartial q = partials[i];
+        s = __dadd_rn(s, __dadd_rn(__dadd_rn(static_cast<double>(q.hi), static_cast<double>(q.lo)), q.wide));
+    }
+    s = block_sum(s, smem);
     if (threadIdx.x == 0) {
+        block_sums[blockIdx.x] = s;
+        __threadfence();  // the sum is visible before the count says so
+        last = atomicAdd(done, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    const double x = threadIdx.x < gridDim.x ? *reinterpret_cast<volatile double *>(&block_sums[threadIdx.x]) : 0.0;
+    __syncthreads();  // smem is reused by the second tree
+    const double S = block_sum(x, smem);
+    if (threadIdx.x == 0) {
+        *done = 0u;
         *sqnorm_ws = S;
         if (sqnorm_out != nullptr) *sqnorm_out = S;
         if (max_norm > 0.0f) {
@@ -994,10 +1036,10 @@ struct PipeGeometry {
 // ZERO_PIPE_MIN_STAGES stages would not fit the shared-memory budget; then as
 // many stages as fit.  (A tile below the pass width leaves some consumer
 // threads without work in a pass; the loop allows any multiple of 8.)
-static PipeGeometry pipe_geometry(int mode, int n_ranks, int gdtype) {
+static PipeGeometry pipe_geometry(int mode, int n_ranks, int gdtype, int cw) {
     const int gb = gdtype == ZERO_BF16 ? 2 : 4;
     const size_t per_elem = mode == MODE_SHARD ? 16 : static_cast<size_t>(n_ranks) * gb + (mode == MODE_FUSED ? 12 : 0);
-    const size_t quantum = 4 * kConsumerWarps * 32;
+    const size_t quantum = 4 * static_cast<size_t>(cw) * 32;
     const size_t mult = ZERO_PIPE_STAGE_TARGET / (quantum * per_elem);
     int tile = static_cast<int>(quantum * (mult > 0 ? mult : 1));
     while (tile > 64 && static_cast<size_t>(ZERO_PIPE_MIN_STAGES) * stage_layout(mode, n_ranks, gb, tile).bytes >
@@ -1028,7 +1070,11 @@ static int sm_count_current_device(int *out) {
 }
 
 template <int MODE, int GD, int NR>
-static int launch_pipe_one(int64_t nseg, const KParams &kp, const PipeGeometry &g, cudaStream_t st) {
+static int launch_pipe_one(int64_t nseg, KParams &kp, cudaStream_t st) {
+    constexpr int CW = consumer_warps<NR>();
+    const PipeGeometry g = pipe_geometry(MODE, kp.n_ranks, GD, CW);
+    kp.tile = g.tile;
+    kp.stages = g.stages;
     cudaError_t e = cudaFuncSetAttribute(k_pipe<MODE, GD, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(g.smem));
     if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
@@ -1036,29 +1082,29 @@ static int launch_pipe_one(int64_t nseg, const KParams &kp, const PipeGeometry &
     const int rc = sm_count_current_device(&sms);
     if (rc != ZERO_OK) return rc;
     const int64_t grid = nseg < sms ? nseg : sms;
-    k_pipe<MODE, GD, NR><<<static_cast<unsigned>(grid), kPipeThreads, g.smem, st>>>(kp, nseg);
+    k_pipe<MODE, GD, NR><<<static_cast<unsigned>(grid), (CW + 1) * 32, g.smem, st>>>(kp, nseg);
     return launch_status();
 }
 
 template <int MODE>
-static int launch_pipe_mode(int gd, int nr, int64_t nseg, const KParams &kp, const PipeGeometry &g, cudaStream_t st) {
+static int launch_pipe_mode(int gd, int nr, int64_t nseg, KParams &kp, cudaStream_t st) {
     if (gd == ZERO_BF16) {
         switch (nr) {
-            case 1: return launch_pipe_one<MODE, ZERO_BF16, 1>(nseg, kp, g, st);
-            case 2: return launch_pipe_one<MODE, ZERO_BF16, 2>(nseg, kp, g, st);
-            case 4: return launch_pipe_one<MODE, ZERO_BF16, 4>(nseg, kp, g, st);
-            case 8: return launch_pipe_one<MODE, ZERO_BF16, 8>(nseg, kp, g, st);
-            case 16: return launch_pipe_one<MODE, ZERO_BF16, 16>(nseg, kp, g, st);
-            default: return launch_pipe_one<MODE, ZERO_BF16, 0>(nseg, kp, g, st);
+            case 1: return launch_pipe_one<MODE, ZERO_BF16, 1>(nseg, kp, st);
+            case 2: return launch_pipe_one<MODE, ZERO_BF16, 2>(nseg, kp, st);
+            case 4: return launch_pipe_one<MODE, ZERO_BF16, 4>(nseg, kp, st);
+            case 8: return launch_pipe_one<MODE, ZERO_BF16, 8>(nseg, kp, st);
+            case 16: return launch_pipe_one<MODE, ZERO_BF16, 16>(nseg, kp, st);
+            default: return launch_pipe_one<MODE, ZERO_BF16, 0>(nseg, kp, st);
         }
     }
     switch (nr) {
-        case 1: return launch_pipe_one<MODE, ZERO_F32, 1>(nseg, kp, g, st);
-        case 2: return launch_pipe_one<MODE, ZERO_F32, 2>(nseg, kp, g, st);
-        case 4: return launch_pipe_one<MODE, ZERO_F32, 4>(nseg, kp, g, st);
-        case 8: return launch_pipe_one<MODE, ZERO_F32, 8>(nseg, kp, g, st);
-        case 16: return launch_pipe_one<MODE, ZERO_F32, 16>(nseg, kp, g, st);
-        default: return launch_pipe_one<MODE, ZERO_F32, 0>(nseg, kp, g, st);
+        case 1: return launch_pipe_one<MODE, ZERO_F32, 1>(nseg, kp, st);
+        case 2: return launch_pipe_one<MODE, ZERO_F32, 2>(nseg, kp, st);
+        case 4: return launch_pipe_one<MODE, ZERO_F32, 4>(nseg, kp, st);
+        case 8: return launch_pipe_one<MODE, ZERO_F32, 8>(nseg, kp, st);
+        case 16: return launch_pipe_one<MODE, ZERO_F32, 16>(nseg, kp, st);
+        default: return launch_pipe_one<MODE, ZERO_F32, 0>(nseg, kp, st);
     }
 }
 
@@ -1068,21 +1114,24 @@ static std::atomic<int64_t> g_drop_tile{-1};
 int launch_pipe(int mode, int gd, int64_t nseg, KParams &kp, cudaStream_t st) {
     if (nseg <= 0) return ZERO_OK;
     kp.drop_tile = g_drop_tile.exchange(-1);
-    const PipeGeometry g = pipe_geometry(mode, kp.n_ranks, gd);
-    kp.tile = g.tile;
-    kp.stages = g.stages;
     switch (mode) {
-        case MODE_FUSED: return launch_pipe_mode<MODE_FUSED>(gd, kp.n_ranks, nseg, kp, g, st);
-        case MODE_REDUCE: return launch_pipe_mode<MODE_REDUCE>(gd, kp.n_ranks, nseg, kp, g, st);
-        default: return launch_pipe_one<MODE_SHARD, ZERO_F32, 1>(nseg, kp, g, st);  // no gradient rows: one instance
+        case MODE_FUSED: return launch_pipe_mode<MODE_FUSED>(gd, kp.n_ranks, nseg, kp, st);
+        case MODE_REDUCE: return launch_pipe_mode<MODE_REDUCE>(gd, kp.n_ranks, nseg, kp, st);
+        default: return launch_pipe_one<MODE_SHARD, ZERO_F32, 1>(nseg, kp, st);  // no gradient rows: one instance
     }
 }
 
 void arm_drop_tile(int64_t tile) { g_drop_tile.store(tile); }
 
-int launch_finalize(const double *partials, int64_t nseg, float max_norm, double *sqnorm_ws, double *sqnorm_out,
-                    float *coef_out, int *skipped, cudaStream_t st) {
-    k_finalize<<<1, kFinThreads, 0, st>>>(partials, nseg, max_norm, sqnorm_ws, sqnorm_out, coef_out, skipped);
+int launch_finalize(const zero_plan *plan, float max_norm, double *sqnorm_out, cudaStream_t st) {
+    const int64_t n = static_cast<int64_t>(plan->segs.size()) * kPartialSlots;
+    // blocks of a whole number of passes, at most kFinBlocks of them (at least one, for S = 0)
+    int64_t block = (n + kFinBlocks - 1) / kFinBlocks;
+    block = block > 0 ? (block + kFinThreads - 1) / kFinThreads * kFinThreads : kFinThreads;
+    const int64_t blocks = n > 0 ? (n + block - 1) / block : 1;
+    k_finalize<<<static_cast<unsigned>(blocks), kFinThreads, 0, st>>>(
+        plan->d_partials, n, block, max_norm, plan->d_fin_sums, plan->d_fin_count, plan->d_sqnorm, sqnorm_out,
+        plan->d_coef, plan->d_skipped);
     return launch_status();
 }
 

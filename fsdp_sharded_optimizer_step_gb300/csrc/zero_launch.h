@@ -29,7 +29,7 @@ struct KParams {
     AdamConsts c;
     float coef;             // host clip coefficient (reduce-scatter); 1 = none
     int32_t write_g, want_partials, use_coef_dev;
-    double *partials;       // per segment, indexed by absolute segment number
+    SqPartial *partials;    // kPartialSlots per segment, indexed by absolute segment number
     int *err;               // device error word (a bounded wait expired)
     int32_t tile, stages;   // pipeline geometry of k_pipe
     int64_t p_pad, h_len;   // element counts of full-length and shard buffers
@@ -54,11 +54,10 @@ int launch_status();
 // (fills the pipeline geometry into kp).
 int launch_pipe(int mode, int gd, int64_t nseg, KParams &kp, cudaStream_t st);
 
-// Fixed-order total of nseg per-segment partials into *sqnorm_ws (and
-// *sqnorm_out); with max_norm > 0 also the clip coefficient (NaN and *skipped
-// = 1 when the total is not finite).
-int launch_finalize(const double *partials, int64_t nseg, float max_norm, double *sqnorm_ws, double *sqnorm_out,
-                    float *coef_out, int *skipped, cudaStream_t st);
+// Fixed-order total of all of the plan's per-segment partials into its S
+// (and *sqnorm_out, a device binary64, when not null); with max_norm > 0 also
+// the clip coefficient (NaN and the skipped flag set when S is not finite).
+int launch_finalize(const zero_plan *plan, float max_norm, double *sqnorm_out, cudaStream_t st);
 
 // Gather of `count` segments from kp.seg_base: rank shards (kp.pshard) into kp.full.
 int launch_gather(int64_t count, const KParams &kp, cudaStream_t st);

@@ -18,6 +18,7 @@
 #include <unordered_map>
 
 #include "zero_internal.h"
+#include "zero_nvtx.h"
 
 namespace {
 
@@ -130,6 +131,7 @@ bool on_device(const void *ptr, int dev) {
 
 extern "C" int zero_grad_sqnorm_noalloc(const void *const *grads, int32_t n_ranks, int32_t gdtype, int64_t n,
                                         double *sqnorm_dev, zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     if (grads == nullptr || sqnorm_dev == nullptr || n < 0) return ZERO_EINVAL;
     if (n_ranks < 1 || n_ranks > ZERO_MAX_RANKS) return ZERO_EINVAL;
     if (gdtype != ZERO_BF16 && gdtype != ZERO_F32) return ZERO_EINVAL;

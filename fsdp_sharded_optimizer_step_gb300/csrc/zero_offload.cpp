@@ -35,6 +35,7 @@
 #include <vector>
 
 #include "zero_launch.h"
+#include "zero_nvtx.h"
 
 namespace zero {
 namespace {
@@ -355,6 +356,7 @@ extern "C" void zero_offload_destroy(zero_offload *eng) { delete eng; }
 extern "C" int zero_offload_adamw(zero_offload *eng, const float *const *gshard_h, float *const *master_h,
                                   float *const *m_h, float *const *v_h, void *const *pshard_h, void *full_h,
                                   int32_t pdtype, const zero_hparams *hp, double sqnorm, int32_t unit) {
+    ZERO_NVTX_RANGE();
     if (eng == nullptr || hp == nullptr) return ZERO_EINVAL;
     const zero_plan *plan = eng->plan;
     if (pdtype != ZERO_BF16 && pdtype != ZERO_F32) return ZERO_EINVAL;
@@ -388,6 +390,7 @@ extern "C" int zero_offload_step(zero_offload *eng, const void *const *grads, in
                                  float *const *gshard_dev, float *const *gshard_h, float *const *master_h,
                                  float *const *m_h, float *const *v_h, void *full_h, void *full_dev, int32_t pdtype,
                                  const zero_hparams *hp, double *sqnorm_out, zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     const auto t_call = std::chrono::steady_clock::now();
     if (eng == nullptr || hp == nullptr) return ZERO_EINVAL;
     const zero_plan *plan = eng->plan;
@@ -437,10 +440,7 @@ extern "C" int zero_offload_step(zero_offload *eng, const void *const *grads, in
         double S = 0.0;
         if (clip) {
             // the fixed-order total of every segment's sum of squares, read back once
-            const int64_t nseg = static_cast<int64_t>(plan->segs.size());
-            if ((rc = launch_finalize(plan->d_partials, nseg, hp->max_norm, plan->d_sqnorm, nullptr, plan->d_coef,
-                                      plan->d_skipped, st)) != ZERO_OK)
-                return rc;
+            if ((rc = launch_finalize(plan, hp->max_norm, nullptr, st)) != ZERO_OK) return rc;
             if ((e = cudaMemcpyAsync(eng->host_S, plan->d_sqnorm, sizeof(double), cudaMemcpyDeviceToHost, st)) !=
                 cudaSuccess)
                 return cuda_fail(e);

@@ -20,9 +20,10 @@ WsLayout workspace_layout(const zero_plan *plan) {
     const size_t nseg = plan->segs.size();
     L.segs = 0;
     L.partials = round_up(nseg * sizeof(Seg), 256);
-    L.scalars = L.partials + round_up(nseg * sizeof(double), 256);
+    L.scalars = L.partials + round_up(nseg * zero::kPartialSlots * sizeof(zero::SqPartial), 256);
     L.units = L.scalars + 256;
-    L.total = L.units + round_up(plan->unit_table.size() * sizeof(UnitDesc), 256);
+    L.fin = L.units + round_up(plan->unit_table.size() * sizeof(UnitDesc), 256);
+    L.total = L.fin + round_up(zero::kFinBlocks * sizeof(double), 256);
     return L;
 }
 
@@ -98,9 +99,10 @@ extern "C" int zero_plan_create(const int64_t *unit_sizes, int32_t n_units, int3
         }
         p->p_pad = full;
         p->H = shard;
-        // Launch table: slices cut into segments of at most kSegMax elements;
-        // the first segment of a slice ends where the shard position reaches a
-        // multiple of 8, so every later segment starts 32-byte aligned.
+        // Launch table: slices cut into segments of at most seg_max_for(N)
+        // elements; the first segment of a slice ends where the shard position
+        // reaches a multiple of 8, so every later segment starts 32-byte aligned.
+        const int64_t seg_max = zero::seg_max_for(n_ranks);
         for (int32_t u = 0; u < n_units; ++u) {
             p->unit_seg_begin[u] = static_cast<int64_t>(p->segs.size());
             const int64_t hu = p->h[u];
@@ -108,7 +110,7 @@ extern "C" int zero_plan_create(const int64_t *unit_sizes, int32_t n_units, int3
                 int64_t j = 0;
                 while (j < hu) {
                     const int64_t s_off = p->Hoff[u] + j;
-                    int64_t len = zero::kSegMax;
+                    int64_t len = seg_max;
                     if (j == 0) len -= (s_off & 7);
                     if (len > hu - j) len = hu - j;
                     Seg sg;

@@ -15,6 +15,7 @@
 #include <cstdint>
 
 #include "zero_internal.h"
+#include "zero_nvtx.h"
 
 namespace {
 
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(kThreads) k_reshard(const ReshardArgs a) {
 
 extern "C" int zero_reshard(const zero_plan *from, const zero_plan *to, const void *const *src, void *const *dst,
                             int32_t dtype, zero_stream_t stream) {
+    ZERO_NVTX_RANGE();
     if (from == nullptr || to == nullptr || src == nullptr || dst == nullptr) return ZERO_EINVAL;
     if (!from->attached || !to->attached) return ZERO_ENOTATTACHED;
     if (from->device != to->device) return ZERO_EINVAL;
