@@ -802,11 +802,16 @@ def run_unit_flows(args, world, rank, local):
             view.copy_(grads[:, plan.F[u0]:plan.F[u0] + view.shape[1]])
 
         flows = {}
+        state0 = [x.clone() for x in (master, m, v)]
         for label, be in (("one unit per bucket", 1), ("2^26-element buckets", 1 << 26),
                           ("default buckets", None), ("2^28-element buckets", 1 << 28)):
+            for x, x0 in zip((master, m, v), state0):  # every flow starts from the same finite state
+                x.copy_(x0)
             bs = BucketedStep(plan, bucket_elems=be)
-            first = bs.buckets[0]
-            fill(*first, bs.view(*first))
+            # every bucket holds real gradients (the first bucket-length positions of each rank):
+            # uninitialised memory would feed inf/NaN/subnormal values into the state, and the
+            # exact division and square root then take their slow paths in every later launch
+            bs.bucket.copy_(grads[:, :bs.bucket.shape[1]])
 
             def updates():  # the bucket updates alone, back to back (the bucket holds gradients)
                 for u0, u1 in bs.buckets:
@@ -818,7 +823,10 @@ def run_unit_flows(args, world, rank, local):
                                 lambda: bs.step(fill, master, m, v, hp, full=full), stream, reps)}
             del bs
         # the previous flow: per-unit reduce-scatter into the fp32 gradient shard, then the shard update
+        for x, x0 in zip((master, m, v), state0):
+            x.copy_(x0)
         buckets = BucketedReduceScatter(plan)
+        buckets.bucket.copy_(grads[:, :buckets.bucket.shape[1]])
         t_rs = _time_ms(lambda: [Z.zero_reduce_scatter_unit(plan, u, buckets.bucket[:, :plan.S[u]], gshard)
                                  for u in reversed(range(plan.n_units))], stream, reps)
         t_shard = _time_ms(lambda: Z.zero_adamw_shard_step(plan, gshard, master, m, v, hp, full=full), stream, reps)

@@ -270,11 +270,18 @@ __device__ __forceinline__ void sq_reset(SqAcc &a) {
     a.wide = 0.0;
 }
 
+// The binary64 path of the rare values, kept out of line: inlined, the compiler
+// predicates it and issues its binary64 instructions for every element (the
+// binary64 pipe was 44% busy in the norm pass), as a call it runs only when taken.
+__device__ __noinline__ double add_square_wide(double acc, float g) {
+    const double d = static_cast<double>(g);
+    return __dadd_rn(acc, __dmul_rn(d, d));
+}
+
 __device__ __forceinline__ void add_square(SqAcc &a, float g) {
     const float mag = fabsf(g);
     if (!(mag <= 0x1p56f) || (mag < 0x1p-51f && mag != 0.0f)) {
-        const double d = static_cast<double>(g);
-        a.wide = __dadd_rn(a.wide, __dmul_rn(d, d));
+        a.wide = add_square_wide(a.wide, g);
         return;
     }
     const float ph = __fmul_rn(g, g);
@@ -298,6 +305,14 @@ __device__ __forceinline__ void pair_add(float &hi, float &lo, float bhi, float 
     lo = __fsub_rn(t, __fsub_rn(hi, s));
 }
 
+// The binary64 parts added across the warp (lane 0 holds the sum), out of line
+// for the same reason as add_square_wide.
+__device__ __noinline__ double warp_wide(double w) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) w = __dadd_rn(w, __shfl_down_sync(0xFFFFFFFFu, w, o));
+    return w;
+}
+
 // A warp's accumulators added across the warp (a fixed shuffle tree; lane 0
 // holds the result): the pair in binary32 pair arithmetic, the binary64 part only
 // when some lane has one (values outside the pair's range are rare).
@@ -309,10 +324,7 @@ __device__ __forceinline__ SqPartial warp_sq(const SqAcc &a) {
         const float olo = __shfl_down_sync(0xFFFFFFFFu, r.lo, o);
         pair_add(r.hi, r.lo, ohi, olo);
     }
-    if (__any_sync(0xFFFFFFFFu, __double_as_longlong(r.wide) != 0)) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) r.wide = __dadd_rn(r.wide, __shfl_down_sync(0xFFFFFFFFu, r.wide, o));
-    }
+    if (__any_sync(0xFFFFFFFFu, __double_as_longlong(r.wide) != 0)) r.wide = warp_wide(r.wide);
     return r;
 }
 
