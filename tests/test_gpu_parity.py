@@ -628,6 +628,27 @@ def test_zero2_bucketed_step_bit_exact(bucket_elems, max_norm):
     assert covered == [u for u in range(len(sizes)) if c.plan.S[u] or u in covered]
 
 
+@pytest.mark.slow
+def test_gpt2l_zero2_bucketed_full_size_sampled():
+    """The bucketed ZeRO-2 step as the bench times it (GPT-2L, N=8, the default buckets,
+    filled in backward order from the full gradient rows): 300k sampled positions,
+    every slice boundary and one whole block unit against the oracle, two steps."""
+    from fsdp_sharded_optimizer_step_gb300.zero3 import BucketedStep
+    c = SampledCase("gpt2l", n_random=300000, extra_units=(20,))
+    bs = BucketedStep(c.plan)
+    assert len(bs.buckets) == 7 and bs.bucket_bytes < c.grads.shape[0] * c.grads.stride(0) * 2
+
+    def fill(u0, u1, view):
+        F0 = c.plan.F[u0]
+        view.copy_(c.grads[:, F0:F0 + view.shape[1]])
+
+    for t in (1, 2):
+        hp, _ = hp_for(t)
+        bs.step(fill, c.master, c.m, c.v, hp, full=c.full)
+        torch.cuda.synchronize()
+        c.assert_sample_equal(c.oracle_step(t))
+
+
 # ------------------------------------------------------------------ failure detection without a GPU fault
 def test_bounded_wait_runs_out_and_is_reported():
     """A pipeline stage that never fills (one tile's copies dropped in the first segment by the
