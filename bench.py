@@ -610,7 +610,7 @@ def run_offload(args, world, rank, local):
     full_h = torch.empty(P, dtype=pdt, pin_memory=True)
     full_dev = torch.empty(P, dtype=pdt, device=dev)
     eng = B.OffloadEngine(plan, n_threads=args.offload_threads, batch_min=args.offload_batch)
-    threads = args.offload_threads or len(os.sched_getaffinity(0))
+    threads, n_batches = Z.zero_offload_info(eng)
     stream = torch.cuda.current_stream(dev)
     max_norm = cfg.get("max_norm", 0.0)
 
@@ -673,8 +673,7 @@ def run_offload(args, world, rank, local):
             "value": world * psi / (ms / 1e3), "unit": "params/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "wall_ms_per_step": wall_ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": dict(workload_config(args.config, cfg, plan), host_threads=threads,
-                           batches=len(eng_batches(plan, args.offload_batch))),
+            "config": dict(workload_config(args.config, cfg, plan), host_threads=threads, batches=n_batches),
             "link": {"d2h_bytes_per_step": d2h_bytes, "h2d_bytes_per_step": h2d_bytes,
                      "d2h_GBps_alone": d2h_bytes / (t_d2h / 1e3) / 1e9, "h2d_GBps_alone": h2d_bytes / (t_h2d / 1e3) / 1e9,
                      "d2h_ms_alone": t_d2h, "h2d_ms_alone": t_h2d},
@@ -685,7 +684,7 @@ def run_offload(args, world, rank, local):
             "breakdown_one_step_ms": tm,
             "share": {"update_on_cores": tm["update_ms"] / tm["device_to_params_ms"],
                       "waiting_for_link": tm["wait_ms"] / tm["device_to_params_ms"]},
-            "gpu_launches": args.steps * len(eng_batches(plan, args.offload_batch)) * (2 if max_norm > 0 else 1),
+            "gpu_launches": args.steps * (n_batches + (1 if max_norm > 0 else 0)),
             "clocks": clock_info}), flush=True)
     return 0
 
@@ -707,21 +706,6 @@ def host_stream_gbps(threads, n=1 << 28, reps=5):
         return 12 * n / best / 1e9
     finally:
         torch.set_num_threads(old)
-
-
-def eng_batches(plan, batch_min):
-    """The engine's batches of consecutive units (at least batch_min padded elements each,
-    2^22 when 0), as the library forms them; for reporting the launch count."""
-    bmin = batch_min or (1 << 22)
-    out, u, U = [], 0, plan.n_units
-    while u < U:
-        u0, elems = u, 0
-        while u < U and (elems < bmin or plan.S[u] == 0):
-            elems += plan.S[u]
-            u += 1
-        if elems:
-            out.append((u0, u))
-    return out
 
 
 def _time_ms(fn, stream, reps, rounds=3, warm=2):

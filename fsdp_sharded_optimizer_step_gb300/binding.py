@@ -99,6 +99,7 @@ def lib():
             "zero_offload_adamw": (C.c_int, [p, pp, pp, pp, pp, pp, p, i32, p, C.c_double, i32]),
             "zero_offload_step": (C.c_int, [p, pp, i32, pp, pp, pp, pp, pp, p, p, i32, p, p, p]),
             "zero_offload_timings": (C.c_int, [p, p]),
+            "zero_offload_info": (C.c_int, [p, p, p]),
             "zero_plan_device_errors": (C.c_int, [p, p, p]),
             "zero_plan_check": (C.c_int, [p, p]),
             "zero_debug_drop_copy": (C.c_int, [i64]),
@@ -571,6 +572,13 @@ def zero_offload_step(eng, grads, gshard_dev, gshard_h, master_h, m_h, v_h, full
     if rc not in (ZERO_OK, ZERO_ENONFINITE):
         _check(rc, "zero_offload_step")
     return rc, (S.value if hp.max_norm > 0 else None)
+
+
+def zero_offload_info(eng):
+    """(host worker threads, pipeline batches) of an engine."""
+    t, b = C.c_int32(), C.c_int64()
+    _check(lib().zero_offload_info(eng.handle, C.byref(t), C.byref(b)), "zero_offload_info")
+    return t.value, b.value
 
 
 def zero_offload_timings(eng):

@@ -224,19 +224,7 @@ struct zero_offload {
     double call_ms = 0, wait_ms = 0, cpu_ms = 0;
     bool stepped = false;
 
-    ~zero_offload() {
-        if (streams_ready) {
-            for (cudaEvent_t e : reduced) cudaEventDestroy(e);
-            for (cudaEvent_t e : landed) cudaEventDestroy(e);
-            cudaEventDestroy(ev_start);
-            cudaEventDestroy(ev_landed);
-            cudaEventDestroy(ev_sent);
-            cudaStreamDestroy(d2h);
-            cudaStreamDestroy(h2d);
-            cudaFreeHost(host_S);
-        }
-        delete pool;
-    }
+    ~zero_offload();
 };
 
 namespace {
@@ -288,25 +276,50 @@ int dev_rows_check(const zero_plan *plan, const void *const *arr) {
     return ZERO_OK;
 }
 
+// Releases the copy streams, events and page-locked scalar (whatever exists).
+void release_device_side(zero_offload *eng) {
+    for (cudaEvent_t &ev : eng->reduced)
+        if (ev != nullptr) cudaEventDestroy(ev), ev = nullptr;
+    for (cudaEvent_t &ev : eng->landed)
+        if (ev != nullptr) cudaEventDestroy(ev), ev = nullptr;
+    for (cudaEvent_t *ev : {&eng->ev_start, &eng->ev_landed, &eng->ev_sent})
+        if (*ev != nullptr) cudaEventDestroy(*ev), *ev = nullptr;
+    for (cudaStream_t *st : {&eng->d2h, &eng->h2d})
+        if (*st != nullptr) cudaStreamDestroy(*st), *st = nullptr;
+    if (eng->host_S != nullptr) cudaFreeHost(eng->host_S), eng->host_S = nullptr;
+    eng->streams_ready = false;
+}
+
+// The copy streams, events and a page-locked scalar, made on the current device by
+// the first step; after a failure nothing is kept and the next step tries again.
 int make_device_side(zero_offload *eng) {
     if (eng->streams_ready) return ZERO_OK;
+    eng->reduced.assign(eng->batches.size(), nullptr);
+    eng->landed.assign(eng->batches.size(), nullptr);
     cudaError_t e = cudaStreamCreateWithFlags(&eng->d2h, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&eng->h2d, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreate(&eng->ev_start);
     if (e == cudaSuccess) e = cudaEventCreate(&eng->ev_landed);
     if (e == cudaSuccess) e = cudaEventCreate(&eng->ev_sent);
     if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void **>(&eng->host_S), 64, cudaHostAllocDefault);
-    eng->reduced.assign(eng->batches.size(), nullptr);
-    eng->landed.assign(eng->batches.size(), nullptr);
     for (size_t b = 0; e == cudaSuccess && b < eng->batches.size(); ++b) {
         e = cudaEventCreateWithFlags(&eng->reduced[b], cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&eng->landed[b], cudaEventDisableTiming);
     }
-    eng->streams_ready = true;  // the destructor releases whatever was made
-    return e == cudaSuccess ? ZERO_OK : cuda_fail(e);
+    if (e != cudaSuccess) {
+        release_device_side(eng);
+        return cuda_fail(e);
+    }
+    eng->streams_ready = true;
+    return ZERO_OK;
 }
 
 }  // namespace
+
+zero_offload::~zero_offload() {
+    release_device_side(this);
+    delete pool;
+}
 
 extern "C" int zero_offload_create(const zero_plan *plan, int32_t n_threads, int64_t batch_min, zero_offload **out) {
     if (out == nullptr) return ZERO_EINVAL;
@@ -352,6 +365,13 @@ extern "C" int zero_offload_create(const zero_plan *plan, int32_t n_threads, int
 }
 
 extern "C" void zero_offload_destroy(zero_offload *eng) { delete eng; }
+
+extern "C" int zero_offload_info(const zero_offload *eng, int32_t *n_threads, int64_t *n_batches) {
+    if (eng == nullptr) return ZERO_EINVAL;
+    if (n_threads != nullptr) *n_threads = eng->pool->size();
+    if (n_batches != nullptr) *n_batches = static_cast<int64_t>(eng->batches.size());
+    return ZERO_OK;
+}
 
 extern "C" int zero_offload_adamw(zero_offload *eng, const float *const *gshard_h, float *const *master_h,
                                   float *const *m_h, float *const *v_h, void *const *pshard_h, void *full_h,

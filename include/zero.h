@@ -343,6 +343,10 @@ int zero_offload_create(const zero_plan *plan, int32_t n_threads, int64_t batch_
 /* Frees the engine (threads, copy streams, events).  NULL is a no-op. */
 void zero_offload_destroy(zero_offload *eng);
 
+/* The engine's host worker threads and pipeline batches (each batch is one
+ * reduce launch and one host update per step).  Either pointer may be NULL. */
+int zero_offload_info(const zero_offload *eng, int32_t *n_threads, int64_t *n_batches);
+
 /* The update on the host cores alone, on HOST arrays (no GPU involved): for
  * every rank r and every shard position of unit `unit` (-1: all units), AdamW
  * with the averaged gradient gshard_h[r][j] on master_h/m_h/v_h[r][j].

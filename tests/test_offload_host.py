@@ -191,3 +191,15 @@ def test_host_update_rejects_bad_arguments():
         Z.zero_offload_adamw(c.eng, c.gshard[:, :10], c.master, c.m, c.v, hp, full_h=c.full)
     L = Z.lib()
     assert L.zero_offload_create(None, 0, 0, None) == B.ZERO_EINVAL
+
+
+def test_engine_reports_threads_and_batches():
+    """Batches are consecutive units of at least batch_min padded elements, a zero-sized unit
+    joining the batch before it; the engine reports them and its thread count."""
+    plan = Z.ZeroPlan([100, 0, 300, 50, 0, 0, 700, 10], 2)  # padded sizes 100, 0, 300, 50, 0, 0, 700, 10
+    # batch_min 1: {100, 0} {300} {50, 0, 0} {700} {10}; 150: {100, 0, 300} {50, 0, 0, 700} {10};
+    # 400: the same three; 10^6: everything in one
+    for batch_min, want in ((1, 5), (150, 3), (400, 3), (10 ** 6, 1)):
+        eng = B.OffloadEngine(plan, n_threads=3, batch_min=batch_min)
+        assert Z.zero_offload_info(eng) == (3, want), batch_min
+    assert Z.zero_offload_info(B.OffloadEngine(Z.ZeroPlan([], 4)))[1] == 0
