@@ -12,6 +12,8 @@ Orchestration only (streams, events, unit-sized buffers); the gathers,
 reduce-scatters and updates run in the CUDA library (zero_all_gather_unit,
 zero_reduce_scatter_unit, zero_step_units, zero_clip_reduce_units).
 """
+import ctypes
+
 import torch
 
 from . import binding as B
@@ -20,7 +22,12 @@ from . import binding as B
 class UnitGatherer:
     """Gathers one unit at a time from the rank param shards into one of
     `n_buffers` unit-sized buffers; with prefetch, unit k+1 is gathered on a side
-    stream while the caller's compute runs on unit k."""
+    stream while the caller's compute runs on unit k.
+
+    A gather of one GPT-2-Large block moves ~79 MB (~11 us of HBM time), less than
+    a checked call through the binding costs on the host, so the arguments are
+    checked and marshalled once here (shard pointers, buffer pointers, dtype) and
+    each gather is one direct call of zero_all_gather_unit."""
 
     def __init__(self, plan, pshard, dtype=torch.bfloat16, n_buffers=2):
         self.plan, self.pshard = plan, pshard
@@ -32,9 +39,15 @@ class UnitGatherer:
         self.side = torch.cuda.Stream(dev)
         self.ready = [torch.cuda.Event() for _ in range(n_buffers)]
         self.free = [torch.cuda.Event() for _ in range(n_buffers)]
+        self._shards, self._pdtype = B._rows(plan, pshard, plan.H, "pshard", (dtype,))
+        self._dst = [ctypes.c_void_p(buf.data_ptr()) for buf in self.buffers]
+        self._fn = B.lib().zero_all_gather_unit
 
     def _gather(self, u, b, stream):
-        B.zero_all_gather_unit(self.plan, u, self.pshard, self.buffers[b][:self.plan.S[u]], stream=stream)
+        st = ctypes.c_void_p(stream.cuda_stream)
+        rc = self._fn(self.plan.handle, u, self._shards, self._dst[b], self._pdtype, st)
+        if rc != B.ZERO_OK:
+            raise B.ZeroError(rc, "zero_all_gather_unit")
 
     def run(self, compute, order=None, prefetch=True, stream=None):
         """compute(u, params_u) is called for every unit in `order`, on `stream`
