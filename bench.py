@@ -163,10 +163,13 @@ def dist_setup(args):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
+        from datetime import timedelta
         backend = "nccl" if torch.cuda.is_available() and args.impl != "reference" else "gloo"
         if backend == "nccl":
             torch.cuda.set_device(local)
-        dist.init_process_group(backend=backend)
+        # a rank that dies or never arrives makes the others' next collective fail after
+        # dist_timeout seconds instead of hanging (the ranks share no device work)
+        dist.init_process_group(backend=backend, timeout=timedelta(seconds=args.dist_timeout))
     return world, rank, local
 
 
@@ -842,6 +845,8 @@ def main():
                          "region (removes host launch overhead; the step counter t is the one captured)")
     ap.add_argument("--ref-sample", type=int, default=1 << 22)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--dist-timeout", type=float, default=300.0,
+                    help="seconds a rank waits in a collective (barrier, timing reduction) before it fails")
     ap.add_argument("--secondary", action=argparse.BooleanOptionalAction, default=True,
                     help="with the default gpt2l step on one GPU, also time the 4b_z3, 1p3b_clip and finewrap "
                          "workloads (each after the previous one's buffers are freed) into a 'secondary' block")

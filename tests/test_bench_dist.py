@@ -1,6 +1,8 @@
 """The bench's multi-process plumbing on CPU (gloo, world size 2): the
-max-over-ranks timing reduction and barrier, and the reference arm under
-torchrun (rank 0 alone runs and prints one JSON line, the other rank exits 0)."""
+max-over-ranks timing reduction and barrier, a rank that dies before the
+barrier (the survivor fails after the process-group timeout instead of
+hanging), and the reference arm under torchrun (rank 0 alone runs and prints
+one JSON line, the other rank exits 0)."""
 import json
 import os
 import subprocess
@@ -36,6 +38,47 @@ def test_max_over_ranks_gloo_world_2():
         assert p.exitcode == 0
     res = dict(q.get(timeout=10) for _ in range(2))
     assert res == {0: 15.5, 1: 15.5}
+
+
+def _dying_worker(rank, world, port, q):
+    """Rank 1 leaves before the barrier (between steps: it has no work in flight);
+    rank 0 must get an error from its barrier within the timeout, not hang."""
+    import argparse
+    import time
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    bench.dist_setup(argparse.Namespace(impl="reference", dist_timeout=3.0))
+    def report(msg):
+        q.put((rank, msg))
+        q.close()
+        q.join_thread()  # flushed before the process ends without cleanup
+        os._exit(0)
+
+    if rank == 1:
+        report("left")
+    t0 = time.time()
+    try:
+        bench.barrier(world)
+        report("no error")
+    except Exception as e:  # the collective failed: the missing rank was detected
+        report(f"error after {time.time() - t0:.1f} s: {type(e).__name__}")
+
+
+def test_a_rank_that_dies_is_detected_not_waited_for():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29800 + os.getpid() % 1000
+    procs = [ctx.Process(target=_dying_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+    res = dict(q.get(timeout=10) for _ in range(2))
+    assert res[1] == "left"
+    assert res[0].startswith("error after"), res[0]
+    assert float(res[0].split()[2]) < 60.0
 
 
 def _check_reference_line(line, world):
