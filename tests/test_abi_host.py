@@ -154,6 +154,33 @@ def test_argument_errors_are_reported_on_the_host(zlib):
                                            None) == B.ZERO_ENOTATTACHED
     assert L.zero_clip_finalize(None, C.c_float(1.0), None, None) == B.ZERO_EINVAL
     assert L.zero_plan_check(None, None) == B.ZERO_EINVAL
+    # bucket-local calls
+    assert L.zero_step_units(h, 0, 2, ptrs, B.ZERO_BF16, ptrs, ptrs, ptrs, None, None, B.ZERO_BF16, C.byref(hp),
+                             None) == B.ZERO_ENOTATTACHED
+    assert L.zero_step_units(h, 0, 2, ptrs, B.ZERO_BF16, ptrs, ptrs, ptrs, None, None, B.ZERO_BF16, C.byref(clip),
+                             None) == B.ZERO_EINVAL  # no clipping from a bucket
+    assert L.zero_clip_reduce_units(h, 0, 2, ptrs, B.ZERO_BF16, ptrs, None) == B.ZERO_ENOTATTACHED
+    assert L.zero_clip_reduce_units(None, 0, 2, ptrs, B.ZERO_BF16, ptrs, None) == B.ZERO_EINVAL
+    # the offload engine: creation and the host update need no device, the step needs an attached plan
+    eng = C.c_void_p()
+    assert L.zero_offload_create(None, 0, 0, C.byref(eng)) == B.ZERO_EINVAL
+    assert L.zero_offload_create(h, -1, 0, C.byref(eng)) == B.ZERO_EINVAL
+    assert L.zero_offload_create(h, 2, -5, C.byref(eng)) == B.ZERO_EINVAL
+    assert L.zero_offload_create(h, 2, 0, C.byref(eng)) == B.ZERO_OK
+    threads, batches = C.c_int32(), C.c_int64()
+    assert L.zero_offload_info(eng, C.byref(threads), C.byref(batches)) == B.ZERO_OK
+    assert (threads.value, batches.value) == (2, 1)
+    assert L.zero_offload_step(eng, ptrs, B.ZERO_BF16, ptrs, ptrs, ptrs, ptrs, ptrs, C.c_void_p(64), None,
+                               B.ZERO_BF16, C.byref(hp), None, None) == B.ZERO_ENOTATTACHED
+    assert L.zero_offload_adamw(eng, ptrs, ptrs, ptrs, ptrs, None, None, 7, C.byref(hp), C.c_double(0.0),
+                                -1) == B.ZERO_EINVAL  # dtype
+    assert L.zero_offload_adamw(eng, ptrs, ptrs, ptrs, ptrs, None, None, B.ZERO_BF16, C.byref(hp), C.c_double(0.0),
+                                2) == B.ZERO_EINVAL  # unit out of range
+    assert L.zero_offload_adamw(eng, None, ptrs, ptrs, ptrs, None, None, B.ZERO_BF16, C.byref(hp), C.c_double(0.0),
+                                -1) == B.ZERO_EINVAL  # missing gradient shard
+    assert L.zero_offload_timings(eng, (C.c_double * 5)()) == B.ZERO_EINVAL  # no step has run
+    L.zero_offload_destroy(eng)
+    L.zero_offload_destroy(None)
     L.zero_plan_destroy(h)
     L.zero_plan_destroy(None)
 
