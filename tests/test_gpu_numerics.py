@@ -100,12 +100,13 @@ def test_subnormal_and_extreme_values_bit_exact(sizes, N, gd, pd):
         c.assert_pshard_equal()
 
 
-@pytest.mark.parametrize("lo,hi", [(-62, -45), (-149, -126), (-55, -50)])
+@pytest.mark.parametrize("lo,hi", [(-62, -45), (-149, -126), (-55, -50), (40, 70), (-80, 100)])
 def test_clipped_step_with_tiny_gradients(lo, hi):
-    """Gradients whose squares are far below 1 (down to subnormal gradients):
-    the sum of squares stays within 1e-12 of the exact sum, the clip
-    coefficient and the whole update are bit-exact.  max_norm is small enough
-    that the coefficient is below 1, so g*coef is a product of tiny values."""
+    """Gradients whose squares are far below 1 (down to subnormal gradients), or
+    far above it (|g| past 2^56, where the binary32 pair accumulation hands over
+    to binary64), or both in one buffer: the sum of squares stays within 1e-12 of
+    the exact sum, the clip coefficient and the whole update are bit-exact.
+    max_norm is half the norm, so the coefficient is about one half."""
     sizes = [70001, 3, 65537, 12345]
     N = 8
     c = SmallCase(sizes, N, W.F32, W.BF16, seed=lo * 7 + hi)
