@@ -168,9 +168,9 @@ int zero_reduce_scatter(const zero_plan *plan, const void *const *grads, int32_t
  * notes; "ZeRO: Three Ledgers, Zero Redundancy", section 2): writes
  * S = sum over all positions of g^2 (g the averaged gradient, pads 0) as a
  * binary64 to *sqnorm_dev (DEVICE pointer, 8-byte aligned), asynchronously.
- * Each segment's partial sum goes to the plan's workspace, then one fixed-order
- * pass adds them: the result is deterministic, within a few binary64 ulps of
- * the exact sum. */
+ * Each segment's partial sums go to the plan's workspace, then one launch adds
+ * them in a fixed order: the result is the same bits on every run and every
+ * GPU, within about 1e-13 relative of the exact sum. */
 int zero_grad_sqnorm(const zero_plan *plan, const void *const *grads, int32_t gdtype,
                      double *sqnorm_dev, zero_stream_t stream);
 
@@ -275,8 +275,8 @@ int zero_reduce_scatter_unit(const zero_plan *plan, int32_t unit, const void *co
  *    from unit-local gradient buffers (as zero_step_unit): writes the unit's
  *    averaged fp32 gradient into gshard[r][Hoff_u + j] and the sums of squares
  *    of the unit's launch-table segments into the plan's workspace.
- * 2. zero_clip_finalize: adds every segment's sum in table order (the same
- *    fixed order as zero_step) into S (*sqnorm_dev, DEVICE, 8-byte aligned,
+ * 2. zero_clip_finalize: adds every segment's partial sums in a fixed order
+ *    (the same order as zero_step's) into S (*sqnorm_dev, DEVICE, 8-byte aligned,
  *    optional) and the clip coefficient min(1, max_norm / (sqrt(S) + 1e-6)),
  *    both kept on the device; S not finite skips the update of step 3 (and
  *    zero_plan_check then reports ZERO_ENONFINITE).
