@@ -35,11 +35,11 @@ def lib():
         _lib = C.CDLL(os.environ.get("ZERO_ORACLE_LIB") or _build.build())
         p, i32, i64, f32, f64 = C.c_void_p, C.c_int32, C.c_int64, C.c_float, C.c_double
         sig = {
-            "orc_plan": (C.c_int, [p, i32, i32, p, p, p, p, p]),
-            "orc_shard_map": (C.c_int, [p, i32, i32, p]),
-            "orc_pad_mask": (C.c_int, [p, i32, i32, p]),
-            "orc_locate": (C.c_int, [p, i32, i32, i64, p, p, p, p]),
-            "orc_reshard": (C.c_int, [p, i32, i32, i32, i32, p, p]),
+            "orc_plan": (C.c_int, [p, i32, i32, i32, p, p, p, p, p]),
+            "orc_shard_map": (C.c_int, [p, i32, i32, i32, p]),
+            "orc_pad_mask": (C.c_int, [p, i32, i32, i32, p]),
+            "orc_locate": (C.c_int, [p, i32, i32, i32, i64, p, p, p, p]),
+            "orc_reshard": (C.c_int, [p, i32, i32, i32, i32, i32, i32, p, p]),
             "orc_avg_grad_array": (C.c_int, [i64, i32, p, i32, p, p]),
             "orc_bf16_rne": (C.c_uint16, [f32]),
             "orc_bf16_rne_array": (None, [i64, p, p]),
@@ -74,25 +74,27 @@ def _check(rc, what):
 
 # ---------------------------------------------------------------- layout
 class Plan:
-    """Integer layout of the padded flat buffers (S, h, F, Hoff, P_pad, H)."""
+    """Integer layout of the padded flat buffers (S, h, F, Hoff, P_pad, H); align > 1
+    pads every unit to a multiple of N*align (slice lengths multiples of align)."""
 
-    def __init__(self, sizes, n_ranks):
+    def __init__(self, sizes, n_ranks, align=1):
         self.sizes = np.ascontiguousarray(sizes, dtype=np.int64)
         self.N = int(n_ranks)
+        self.align = int(align)
         U = len(self.sizes)
         self.S = np.zeros(U, np.int64)
         self.h = np.zeros(U, np.int64)
         self.F = np.zeros(U, np.int64)
         self.Hoff = np.zeros(U, np.int64)
         tot = np.zeros(2, np.int64)
-        _check(lib().orc_plan(_ptr(self.sizes), U, self.N, _ptr(self.S), _ptr(self.h), _ptr(self.F),
+        _check(lib().orc_plan(_ptr(self.sizes), U, self.N, self.align, _ptr(self.S), _ptr(self.h), _ptr(self.F),
                               _ptr(self.Hoff), _ptr(tot)), "plan")
         self.P_pad, self.H = int(tot[0]), int(tot[1])
 
     def shard_map(self):
         """map[r, p] = full-buffer position stored at position p of rank r's shard."""
         out = np.zeros(self.N * self.H, np.int64)
-        _check(lib().orc_shard_map(_ptr(self.sizes), len(self.sizes), self.N, _ptr(out)), "shard_map")
+        _check(lib().orc_shard_map(_ptr(self.sizes), len(self.sizes), self.N, self.align, _ptr(out)), "shard_map")
         return out.reshape(self.N, self.H)
 
     def locate(self, pos):
@@ -101,25 +103,27 @@ class Plan:
         rank = np.zeros(pos.size, np.int32)
         spos = np.zeros(pos.size, np.int64)
         pad = np.zeros(pos.size, np.uint8)
-        _check(lib().orc_locate(_ptr(self.sizes), len(self.sizes), self.N, pos.size, _ptr(pos), _ptr(rank), _ptr(spos),
+        _check(lib().orc_locate(_ptr(self.sizes), len(self.sizes), self.N, self.align, pos.size, _ptr(pos), _ptr(rank),
+                                _ptr(spos),
                                 _ptr(pad)), "locate")
         return rank, spos, pad
 
     def pad_mask(self):
         out = np.zeros(self.P_pad, np.uint8)
-        _check(lib().orc_pad_mask(_ptr(self.sizes), len(self.sizes), self.N, _ptr(out)), "pad_mask")
+        _check(lib().orc_pad_mask(_ptr(self.sizes), len(self.sizes), self.N, self.align, _ptr(out)), "pad_mask")
         return out
 
 
-def reshard(sizes, n_from, n_to, src):
+def reshard(sizes, n_from, n_to, src, align_from=1, align_to=1):
     """src: [n_from, H_from] array (float32 or uint16 bits) -> [n_to, H_to] in the target layout."""
     sizes = np.ascontiguousarray(sizes, np.int64)
     src = np.ascontiguousarray(src)
-    H_to = Plan(sizes, n_to).H
+    H_to = Plan(sizes, n_to, align_to).H
     dst = np.zeros((n_to, H_to), src.dtype)
     sp = (C.c_void_p * n_from)(*[src[r].ctypes.data for r in range(n_from)])
     dp = (C.c_void_p * n_to)(*[dst[r].ctypes.data for r in range(n_to)])
-    _check(lib().orc_reshard(_ptr(sizes), len(sizes), n_from, n_to, src.dtype.itemsize, sp, dp), "reshard")
+    _check(lib().orc_reshard(_ptr(sizes), len(sizes), n_from, align_from, n_to, align_to, src.dtype.itemsize, sp, dp),
+           "reshard")
     return dst
 
 

@@ -54,16 +54,26 @@ typedef struct {
  * h_u = S_u / N (slice length), F_u = sum_{k<u} S_k (offset of the unit in the
  * full flat buffer), Hoff_u = sum_{k<u} h_k (offset of the unit's slice inside
  * every rank's shard buffer).  totals[0] = P_pad = sum S_u, totals[1] = H =
- * P_pad / N.  Rank r owns full positions [F_u + r h_u, F_u + (r+1) h_u). */
-int orc_plan(const int64_t *sizes, int32_t n_units, int32_t n_ranks,
+ * P_pad / N.  Rank r owns full positions [F_u + r h_u, F_u + (r+1) h_u).
+ *
+ * Every layout function takes `align` (>= 1): the padding quantum is N*align
+ * instead of N, so every slice length h_u is a multiple of align.  The pages
+ * fix no alignment; align = 1 is their layout, larger values are an option
+ * (slices that start on whole vectors). */
+static int64_t orc_pad_to(int64_t s, int64_t quantum)
+{
+    int64_t rem = s % quantum;
+    return rem == 0 ? s : s + (quantum - rem);
+}
+
+int orc_plan(const int64_t *sizes, int32_t n_units, int32_t n_ranks, int32_t align,
              int64_t *S, int64_t *h, int64_t *F, int64_t *Hoff, int64_t *totals)
 {
-    if (n_units < 0 || n_ranks < 1) return ORC_EINVAL;
+    if (n_units < 0 || n_ranks < 1 || align < 1) return ORC_EINVAL;
     int64_t f = 0, hh = 0;
     for (int32_t u = 0; u < n_units; ++u) {
         if (sizes[u] < 0) return ORC_EINVAL;
-        int64_t rem = sizes[u] % n_ranks;
-        int64_t padded = rem == 0 ? sizes[u] : sizes[u] + (n_ranks - rem);
+        int64_t padded = orc_pad_to(sizes[u], (int64_t)n_ranks * align);
         S[u] = padded;
         h[u] = padded / n_ranks;
         F[u] = f;
@@ -78,18 +88,15 @@ int orc_plan(const int64_t *sizes, int32_t n_units, int32_t n_ranks,
 
 /* map[r*H + p] = full-buffer position held at position p of rank r's shard
  * buffer (the shard buffer concatenates the rank's slices in unit order). */
-int orc_shard_map(const int64_t *sizes, int32_t n_units, int32_t n_ranks, int64_t *map)
+int orc_shard_map(const int64_t *sizes, int32_t n_units, int32_t n_ranks, int32_t align, int64_t *map)
 {
-    if (n_units < 0 || n_ranks < 1) return ORC_EINVAL;
+    if (n_units < 0 || n_ranks < 1 || align < 1) return ORC_EINVAL;
+    const int64_t q = (int64_t)n_ranks * align;
     int64_t H = 0;
-    for (int32_t u = 0; u < n_units; ++u) {
-        int64_t rem = sizes[u] % n_ranks;
-        H += (rem == 0 ? sizes[u] : sizes[u] + (n_ranks - rem)) / n_ranks;
-    }
+    for (int32_t u = 0; u < n_units; ++u) H += orc_pad_to(sizes[u], q) / n_ranks;
     int64_t f = 0, hh = 0;
     for (int32_t u = 0; u < n_units; ++u) {
-        int64_t rem = sizes[u] % n_ranks;
-        int64_t Su = rem == 0 ? sizes[u] : sizes[u] + (n_ranks - rem);
+        int64_t Su = orc_pad_to(sizes[u], q);
         int64_t hu = Su / n_ranks;
         for (int32_t r = 0; r < n_ranks; ++r)
             for (int64_t j = 0; j < hu; ++j)
@@ -105,15 +112,16 @@ int orc_shard_map(const int64_t *sizes, int32_t n_units, int32_t n_ranks, int64_
  * position j of unit u's slice, the unit position k = r*h'_u + j taken from
  * the rank that owns k in the source layout; target padding is 0.  Elements
  * are esize raw bytes. */
-int orc_reshard(const int64_t *sizes, int32_t n_units, int32_t n_from, int32_t n_to, int32_t esize,
-                const void *const *src, void *const *dst)
+int orc_reshard(const int64_t *sizes, int32_t n_units, int32_t n_from, int32_t align_from, int32_t n_to,
+                int32_t align_to, int32_t esize, const void *const *src, void *const *dst)
 {
-    if (n_units < 0 || n_from < 1 || n_to < 1 || (esize != 2 && esize != 4)) return ORC_EINVAL;
+    if (n_units < 0 || n_from < 1 || n_to < 1 || align_from < 1 || align_to < 1 || (esize != 2 && esize != 4))
+        return ORC_EINVAL;
     int64_t hh_from = 0, hh_to = 0;
     for (int32_t u = 0; u < n_units; ++u) {
         int64_t s = sizes[u];
-        int64_t S_from = s % n_from == 0 ? s : s + (n_from - s % n_from);
-        int64_t S_to = s % n_to == 0 ? s : s + (n_to - s % n_to);
+        int64_t S_from = orc_pad_to(s, (int64_t)n_from * align_from);
+        int64_t S_to = orc_pad_to(s, (int64_t)n_to * align_to);
         int64_t h_from = S_from / n_from, h_to = S_to / n_to;
         for (int32_t r = 0; r < n_to; ++r)
             for (int64_t j = 0; j < h_to; ++j) {
@@ -133,13 +141,12 @@ int orc_reshard(const int64_t *sizes, int32_t n_units, int32_t n_from, int32_t n
 }
 
 /* pad[i] = 1 where full position i is padding (position >= s_u inside unit u). */
-int orc_pad_mask(const int64_t *sizes, int32_t n_units, int32_t n_ranks, uint8_t *pad)
+int orc_pad_mask(const int64_t *sizes, int32_t n_units, int32_t n_ranks, int32_t align, uint8_t *pad)
 {
-    if (n_units < 0 || n_ranks < 1) return ORC_EINVAL;
+    if (n_units < 0 || n_ranks < 1 || align < 1) return ORC_EINVAL;
     int64_t f = 0;
     for (int32_t u = 0; u < n_units; ++u) {
-        int64_t rem = sizes[u] % n_ranks;
-        int64_t Su = rem == 0 ? sizes[u] : sizes[u] + (n_ranks - rem);
+        int64_t Su = orc_pad_to(sizes[u], (int64_t)n_ranks * align);
         for (int64_t k = 0; k < Su; ++k) pad[f + k] = (uint8_t)(k >= sizes[u]);
         f += Su;
     }
@@ -149,17 +156,16 @@ int orc_pad_mask(const int64_t *sizes, int32_t n_units, int32_t n_ranks, uint8_t
 /* For n full-buffer positions: the owning rank, the position inside that
  * rank's shard buffer, and whether the position is padding.  (Searches the
  * units in order; the same layout as orc_plan.) */
-int orc_locate(const int64_t *sizes, int32_t n_units, int32_t n_ranks, int64_t n, const int64_t *pos,
+int orc_locate(const int64_t *sizes, int32_t n_units, int32_t n_ranks, int32_t align, int64_t n, const int64_t *pos,
                int32_t *rank, int64_t *shard_pos, uint8_t *is_pad)
 {
-    if (n_units < 0 || n_ranks < 1 || n < 0) return ORC_EINVAL;
+    if (n_units < 0 || n_ranks < 1 || align < 1 || n < 0) return ORC_EINVAL;
     /* the layout of every unit once: F (full offset), S (padded size), h (slice), Hoff */
     int64_t *t = (int64_t *)malloc(sizeof(int64_t) * 4 * (size_t)(n_units > 0 ? n_units : 1));
     if (t == NULL) return ORC_EINVAL;
     int64_t f = 0, hh = 0;
     for (int32_t u = 0; u < n_units; ++u) {
-        int64_t rem = sizes[u] % n_ranks;
-        int64_t Su = rem == 0 ? sizes[u] : sizes[u] + (n_ranks - rem);
+        int64_t Su = orc_pad_to(sizes[u], (int64_t)n_ranks * align);
         t[4 * u] = f;
         t[4 * u + 1] = Su;
         t[4 * u + 2] = Su / n_ranks;

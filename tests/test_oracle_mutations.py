@@ -24,8 +24,7 @@ MUTANTS = [
     ("eps_inside_sqrt", "(sqrtf(vi) / bc2 + hp->eps)", "(sqrtf(vi + hp->eps) / bc2)"),
     ("bf16_truncates", "if (lo > 0x8000u || (lo == 0x8000u && (hi & 1u))) hi += 1u;", "(void)lo;"),
     ("bf16_ties_away", "if (lo > 0x8000u || (lo == 0x8000u && (hi & 1u))) hi += 1u;", "if (lo >= 0x8000u) hi += 1u;"),
-    ("pad_always", "int64_t padded = rem == 0 ? sizes[u] : sizes[u] + (n_ranks - rem);",
-     "int64_t padded = sizes[u] + (n_ranks - rem);"),
+    ("pad_always", "return rem == 0 ? s : s + (quantum - rem);", "return s + (quantum - rem);"),
     ("pads_not_masked", "if (pad != NULL && pad[i]) return 0.0f;", ""),
     ("slice_stride", "map[(int64_t)r * H + hh + j] = f + (int64_t)r * hu + j;", "map[(int64_t)r * H + hh + j] = f + (int64_t)j * n_ranks + r;"),
     ("sqnorm_sum_in_float", "orc_sqacc_add_square(a, orc_avg_grad(n_ranks, grads, gdtype, pad, i));",

@@ -439,20 +439,24 @@ def test_clip_off_equals_no_clip_when_inside_ball(orc):
 # Layout ("ZeRO and FSDP sharding", How it works and Pitfalls; "Learn: ZeRO &
 # FSDP", section 5).  Brute force over unit lists and N: every unit padded to
 # the next multiple of N, slices tile each unit once, the shard map is a
-# permutation, pads are the trailing S_u - s_u positions of each unit.
+# permutation, pads are the trailing S_u - s_u positions of each unit.  The
+# alignment option (align > 1, not on the pages) pads to the next multiple of
+# N*align instead, so every slice length is a multiple of align.
+@pytest.mark.parametrize("align", [1, 2, 8])
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 7, 8, 13, 16])
-def test_plan_brute_force(orc, N):
-    rng = np.random.default_rng(N)
+def test_plan_brute_force(orc, N, align):
+    rng = np.random.default_rng(N * 10 + align)
+    q = N * align
     for trial in range(30):
         U = int(rng.integers(1, 12))
         sizes = rng.integers(0, 60, U)
         sizes[rng.random(U) < 0.2] = 0
-        p = orc.Plan(sizes, N)
+        p = orc.Plan(sizes, N, align)
         for u in range(U):
             s = int(sizes[u])
-            assert p.S[u] % N == 0 and s <= p.S[u] < s + N
-            assert p.S[u] == min(k for k in range(s, s + N) if k % N == 0)
-            assert p.h[u] * N == p.S[u]
+            assert p.S[u] % q == 0 and s <= p.S[u] < s + q
+            assert p.S[u] == min(k for k in range(s, s + q) if k % q == 0)
+            assert p.h[u] * N == p.S[u] and p.h[u] % align == 0
             assert p.F[u] == sum(p.S[:u]) and p.Hoff[u] == sum(p.h[:u])
         assert p.P_pad == sum(p.S) and p.H * N == p.P_pad
         mp = p.shard_map()
@@ -495,6 +499,8 @@ def test_plan_rejects_bad_input(orc):
         orc.Plan([5, -1], 2)
     with pytest.raises(RuntimeError):
         orc.Plan([5], 0)
+    with pytest.raises(RuntimeError):
+        orc.Plan([5], 2, 0)
 
 
 # ----------------------------------------------------------------------------
@@ -531,8 +537,8 @@ def test_toy_optimizer_floats_per_rank(orc):
 # sharded checkpoint is resharded to a different N at load time).  Pinned to
 # the composition of the two (already pinned) layout maps through the unit
 # positions, and to round trips.
-def _reshard_by_maps(orc, sizes, n_from, n_to, src):
-    pf, pt = orc.Plan(sizes, n_from), orc.Plan(sizes, n_to)
+def _reshard_by_maps(orc, sizes, n_from, n_to, src, a_from=1, a_to=1):
+    pf, pt = orc.Plan(sizes, n_from, a_from), orc.Plan(sizes, n_to, a_to)
     full_from = np.zeros(pf.P_pad, src.dtype)
     full_from[pf.shard_map().ravel()] = src.ravel()
     full_to = np.zeros(pt.P_pad, src.dtype)
@@ -550,6 +556,16 @@ def test_reshard_is_the_composition_of_the_layouts(orc, n_from, n_to):
     assert np.array_equal(got.view(np.uint32), _reshard_by_maps(orc, sizes, n_from, n_to, src).view(np.uint32))
     bits = rng.integers(0, 1 << 16, src.shape, dtype=np.int64).astype(np.uint16)
     assert np.array_equal(orc.reshard(sizes, n_from, n_to, bits), _reshard_by_maps(orc, sizes, n_from, n_to, bits))
+
+
+@pytest.mark.parametrize("n_from,a_from,n_to,a_to", [(8, 1, 16, 8), (16, 8, 8, 1), (4, 8, 3, 1), (5, 2, 5, 1)])
+def test_reshard_between_aligned_layouts(orc, n_from, a_from, n_to, a_to):
+    rng = np.random.default_rng(n_from * 7 + a_from * 3 + n_to)
+    sizes = [int(x) for x in rng.integers(0, 300, 9)] + [1, 257]
+    src = rng.normal(0, 1, (n_from, orc.Plan(sizes, n_from, a_from).H)).astype(np.float32)
+    got = orc.reshard(sizes, n_from, n_to, src, align_from=a_from, align_to=a_to)
+    want = _reshard_by_maps(orc, sizes, n_from, n_to, src, a_from, a_to)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
 
 
 def test_reshard_round_trip_and_identity(orc):
