@@ -315,6 +315,8 @@ def workload_config(name, cfg, plan):
          "clip_max_norm": cfg.get("max_norm", 0.0)}
     if plan is not None:
         d["p_pad"] = plan.P_pad
+        if plan.align != 1:
+            d["align"] = plan.align
     return d
 
 
@@ -592,7 +594,7 @@ def run_offload(args, world, rank, local):
     cfg = W.CONFIGS[args.config]
     sizes = cfg["units"]()
     N = cfg["N"]
-    plan = Z.ZeroPlan(sizes, N, dev)
+    plan = Z.ZeroPlan(sizes, N, dev, align=args.align)
     P, H = plan.P_pad, plan.H
     gdt = torch.bfloat16 if cfg["gdtype"] == W.BF16 else torch.float32
     pdt = torch.bfloat16 if cfg["pdtype"] == W.BF16 else torch.float32
@@ -845,6 +847,9 @@ def main():
                          "region (removes host launch overhead; the step counter t is the one captured)")
     ap.add_argument("--ref-sample", type=int, default=1 << 22)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--align", type=int, default=1,
+                    help="pad every unit to a multiple of N*align (slices on align-element boundaries; "
+                         "1 = the pages' layout)")
     ap.add_argument("--dist-timeout", type=float, default=300.0,
                     help="seconds a rank waits in a collective (barrier, timing reduction) before it fails")
     ap.add_argument("--secondary", action=argparse.BooleanOptionalAction, default=True,
@@ -885,7 +890,7 @@ def main():
     cfg = W.CONFIGS[args.config]
     sizes = cfg["units"]()
     N = cfg["N"]
-    plan = Z.ZeroPlan(sizes, N, dev)
+    plan = Z.ZeroPlan(sizes, N, dev, align=args.align)
     P, H = plan.P_pad, plan.H
     gdt = torch.bfloat16 if cfg["gdtype"] == W.BF16 else torch.float32
     pdt = torch.bfloat16 if cfg["pdtype"] == W.BF16 else torch.float32
@@ -964,7 +969,7 @@ def main():
     alg_bytes = bpe * P
     peak, peak_kind = measured_hbm_peak()
     achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
-    traffic = ncu_traffic(args.config, "clip" if clip else "fused") if not args.per_unit else None
+    traffic = ncu_traffic(args.config, "clip" if clip else "fused") if not args.per_unit and args.align == 1 else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic, "peak_kind": peak_kind, "bytes_per_element": bpe,
                 "algorithmic_bytes_per_launch": alg_bytes,
@@ -982,7 +987,7 @@ def main():
 
     # ---------------- the other full-size workloads, each measured after this one's buffers are freed
     secondary = None
-    if world == 1 and args.secondary and args.config == "gpt2l" and not (args.per_unit or args.graph):
+    if world == 1 and args.secondary and args.config == "gpt2l" and args.align == 1 and not (args.per_unit or args.graph):
         del step, grads, master, m, v, full, pshard, gshard, sq, graph
         plan = None
         torch.cuda.empty_cache()

@@ -71,6 +71,8 @@ def lib():
         pp = C.POINTER(C.c_void_p)
         sig = {
             "zero_plan_create": (C.c_int, [p, i32, i32, C.POINTER(C.c_void_p)]),
+            "zero_plan_create_aligned": (C.c_int, [p, i32, i32, i32, C.POINTER(C.c_void_p)]),
+            "zero_plan_align": (C.c_int, [p, p]),
             "zero_plan_destroy": (None, [p]),
             "zero_plan_query": (C.c_int, [p, p, p, p, p, p, p]),
             "zero_plan_counts": (C.c_int, [p, p, p, p]),
@@ -134,6 +136,20 @@ def zero_plan_create(unit_sizes, n_ranks):
     h = C.c_void_p()
     _check(lib().zero_plan_create(sizes, len(unit_sizes), int(n_ranks), C.byref(h)), "zero_plan_create")
     return h
+
+
+def zero_plan_create_aligned(unit_sizes, n_ranks, align):
+    sizes = (C.c_int64 * len(unit_sizes))(*[int(s) for s in unit_sizes])
+    h = C.c_void_p()
+    _check(lib().zero_plan_create_aligned(sizes, len(unit_sizes), int(n_ranks), int(align), C.byref(h)),
+           "zero_plan_create_aligned")
+    return h
+
+
+def zero_plan_align(handle):
+    a = C.c_int32()
+    _check(lib().zero_plan_align(handle, C.byref(a)), "zero_plan_align")
+    return a.value
 
 
 def zero_plan_destroy(handle):
@@ -208,12 +224,15 @@ class ZeroPlan:
     """Owns a plan and its device workspace (a torch uint8 tensor on `device`).
 
     device=None builds the host-side plan only (layout queries work without a
-    GPU; device calls then fail with ZERO_ENOTATTACHED)."""
+    GPU; device calls then fail with ZERO_ENOTATTACHED).  align > 1 pads every
+    unit to a multiple of n_ranks * align (zero_plan_create_aligned)."""
 
-    def __init__(self, unit_sizes, n_ranks, device=None, stream=None):
+    def __init__(self, unit_sizes, n_ranks, device=None, stream=None, align=1):
         self.unit_sizes = [int(s) for s in unit_sizes]
         self.n_ranks = int(n_ranks)
-        self.handle = zero_plan_create(self.unit_sizes, self.n_ranks)
+        self.align = int(align)
+        self.handle = (zero_plan_create(self.unit_sizes, self.n_ranks) if self.align == 1
+                       else zero_plan_create_aligned(self.unit_sizes, self.n_ranks, self.align))
         q = zero_plan_query(self.handle)
         self.P_pad, self.H = q["P_pad"], q["H"]
         self.F, self.Hoff, self.S, self.h = q["F"], q["Hoff"], q["S"], q["h"]

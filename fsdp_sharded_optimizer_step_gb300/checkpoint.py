@@ -4,12 +4,12 @@
 (each rank writes its own shard; gathering the whole state onto one rank is
 slow and can run out of memory) and reshard to a different N when loading.
 
-On disk, a directory holds layout.json (unit sizes, rank count, step, and the
-name/dtype of every array) and one file per rank, rankNNNNN.bin, with that
+On disk, a directory holds layout.json (unit sizes, rank count, alignment,
+step, and the name/dtype of every array) and one file per rank, rankNNNNN.bin, with that
 rank's shard of every array concatenated in layout order.  Loading into a plan
 with another rank count reads the old shards into device buffers and remaps
-them with zero_reshard (one launch per array); the same rank count is a plain
-copy.  Host IO only here: the remap runs in the CUDA library.
+them with zero_reshard (one launch per array); the same rank count and
+alignment is a plain copy.  Host IO only here: the remap runs in the CUDA library.
 """
 import json
 import os
@@ -45,7 +45,8 @@ def save(path, plan, arrays: dict, step: int):
         a = arrays[name]
         if len(a) != plan.n_ranks or any(r.numel() != plan.H for r in a):
             raise ValueError(f"{name}: need {plan.n_ranks} rank rows of {plan.H} elements")
-    layout = {"unit_sizes": plan.unit_sizes, "n_ranks": plan.n_ranks, "H": plan.H, "step": int(step),
+    layout = {"unit_sizes": plan.unit_sizes, "n_ranks": plan.n_ranks, "align": plan.align, "H": plan.H,
+              "step": int(step),
               "arrays": [{"name": n, "dtype": _kind(arrays[n][0])} for n in names]}
     for r in range(plan.n_ranks):
         tmp = os.path.join(path, f"rank{r:05d}.bin.tmp")
@@ -80,8 +81,9 @@ def load(path, plan, stream=None):
 
 
 def _load_arrays(path, layout, plan, dev, stream):
-    n_old, H_old = int(layout["n_ranks"]), int(layout["H"])
-    old = B.ZeroPlan(layout["unit_sizes"], n_old, dev, stream=stream) if n_old != plan.n_ranks else None
+    n_old, H_old, a_old = int(layout["n_ranks"]), int(layout["H"]), int(layout.get("align", 1))
+    same = n_old == plan.n_ranks and a_old == plan.align
+    old = None if same else B.ZeroPlan(layout["unit_sizes"], n_old, dev, stream=stream, align=a_old)
     out = {}
     offset = 0  # bytes into every rank file
     for spec in layout["arrays"]:

@@ -79,6 +79,7 @@ struct AdamConsts {
 
 struct zero_plan {
     int32_t n_units = 0, n_ranks = 0;
+    int32_t align = 1;  // every slice length is a multiple of align (zero_plan_create_aligned)
     std::vector<int64_t> sizes, S, h, F, Hoff;
     int64_t p_pad = 0, H = 0;
     std::vector<zero::Seg> segs;           // host copy of the launch table

@@ -67,15 +67,22 @@ extern "C" int zero_bias_corrections(int32_t t, float b1, float b2, float *bc1, 
 }
 
 extern "C" int zero_plan_create(const int64_t *unit_sizes, int32_t n_units, int32_t n_ranks, zero_plan **out) {
+    return zero_plan_create_aligned(unit_sizes, n_units, n_ranks, 1, out);
+}
+
+extern "C" int zero_plan_create_aligned(const int64_t *unit_sizes, int32_t n_units, int32_t n_ranks, int32_t align,
+                                        zero_plan **out) {
     if (out == nullptr) return ZERO_EINVAL;
     *out = nullptr;
     if (n_units < 0 || (n_units > 0 && unit_sizes == nullptr)) return ZERO_EINVAL;
     if (n_ranks < 1 || n_ranks > ZERO_MAX_RANKS) return ZERO_EINVAL;
+    if (align < 1 || align > ZERO_MAX_ALIGN) return ZERO_EINVAL;
     zero_plan *p = new (std::nothrow) zero_plan();
     if (p == nullptr) return ZERO_ENOMEM;
     try {
         p->n_units = n_units;
         p->n_ranks = n_ranks;
+        p->align = align;
         p->sizes.assign(unit_sizes, unit_sizes + n_units);
         p->S.resize(n_units);
         p->h.resize(n_units);
@@ -84,12 +91,14 @@ extern "C" int zero_plan_create(const int64_t *unit_sizes, int32_t n_units, int3
         p->unit_seg_begin.resize(static_cast<size_t>(n_units) + 1);
         const int64_t limit = int64_t(1) << 62;
         int64_t full = 0, shard = 0;
-        // Padded layout: each unit rounded up to a multiple of N, rank r owning
-        // the r-th of N equal slices ("ZeRO and FSDP sharding", How it works).
+        // Padded layout: each unit rounded up to a multiple of N (of N*align with
+        // the alignment option), rank r owning the r-th of N equal slices ("ZeRO
+        // and FSDP sharding", How it works).
+        const int64_t quantum = static_cast<int64_t>(n_ranks) * align;
         for (int32_t u = 0; u < n_units; ++u) {
             const int64_t s = unit_sizes[u];
-            if (s < 0 || s > limit - full) { delete p; return ZERO_EINVAL; }
-            const int64_t padded = (s + n_ranks - 1) / n_ranks * n_ranks;
+            if (s < 0 || s > limit - full - quantum) { delete p; return ZERO_EINVAL; }
+            const int64_t padded = (s + quantum - 1) / quantum * quantum;
             p->S[u] = padded;
             p->h[u] = padded / n_ranks;
             p->F[u] = full;
@@ -153,6 +162,12 @@ extern "C" int zero_plan_query(const zero_plan *plan, int64_t *p_pad, int64_t *h
     if (Hoff && n) std::memcpy(Hoff, plan->Hoff.data(), n * sizeof(int64_t));
     if (S && n) std::memcpy(S, plan->S.data(), n * sizeof(int64_t));
     if (h_u && n) std::memcpy(h_u, plan->h.data(), n * sizeof(int64_t));
+    return ZERO_OK;
+}
+
+extern "C" int zero_plan_align(const zero_plan *plan, int32_t *align) {
+    if (plan == nullptr || align == nullptr) return ZERO_EINVAL;
+    *align = plan->align;
     return ZERO_OK;
 }
 

@@ -119,6 +119,22 @@ typedef struct {
  * ZERO_ENOMEM. */
 int zero_plan_create(const int64_t *unit_sizes, int32_t n_units, int32_t n_ranks, zero_plan **out);
 
+/* zero_plan_create with an alignment option the pages leave open: every unit is
+ * padded to a multiple of N * align instead of N, so every slice length h_u,
+ * and with it every slice's offset in the full and the shard buffers, is a
+ * multiple of align elements.  align = 8 puts every bf16 slice on a 16-byte
+ * boundary (the kernels then never read a gradient row at a shifted offset);
+ * the cost is at most N * align - 1 more padding positions per unit.  align = 1
+ * is zero_plan_create.  1 <= align <= ZERO_MAX_ALIGN.  Every other call works
+ * on an aligned plan unchanged; zero_reshard maps between plans of any
+ * alignment.  Errors: as zero_plan_create. */
+#define ZERO_MAX_ALIGN 4096
+int zero_plan_create_aligned(const int64_t *unit_sizes, int32_t n_units, int32_t n_ranks, int32_t align,
+                             zero_plan **out);
+
+/* The plan's alignment option (1 for zero_plan_create). */
+int zero_plan_align(const zero_plan *plan, int32_t *align);
+
 /* Frees the plan (host memory only; the caller frees its workspace). NULL is a no-op. */
 void zero_plan_destroy(zero_plan *plan);
 

@@ -116,11 +116,11 @@ class SmallCase:
     """A config small enough that the oracle follows every element."""
 
     def __init__(self, sizes, N, gdtype=W.BF16, pdtype=W.BF16, seed=0, device="cuda", grad_sigma=1e-3,
-                 state="random", outlier_frac=0.0, outlier_scale=1.0):
+                 state="random", outlier_frac=0.0, outlier_scale=1.0, align=1):
         self.sizes, self.N, self.gdtype, self.pdtype = list(sizes), N, gdtype, pdtype
         self.device = torch.device(device)
-        self.plan = Z.ZeroPlan(self.sizes, N, self.device)
-        self.o = O.Plan(self.sizes, N)
+        self.plan = Z.ZeroPlan(self.sizes, N, self.device, align=align)
+        self.o = O.Plan(self.sizes, N, align)
         assert self.plan.P_pad == self.o.P_pad and self.plan.H == self.o.H
         P, H = self.plan.P_pad, self.plan.H
         self.guards = []  # every device buffer below sits between canary bands

@@ -64,11 +64,26 @@ def test_plan_layout_matches_oracle(zlib, orc, sizes, N):
     assert p.F == o.F.tolist() and p.Hoff == o.Hoff.tolist() and p.S == o.S.tolist() and p.h == o.h.tolist()
 
 
+@pytest.mark.parametrize("align", [2, 8, 64])
+@pytest.mark.parametrize("sizes,N", _units_cases()[::4])
+def test_aligned_plan_layout_matches_oracle(zlib, orc, sizes, N, align):
+    p = Z.ZeroPlan(sizes, N, align=align)
+    o = orc.Plan(sizes, N, align)
+    assert Z.zero_plan_align(p.handle) == align
+    assert p.P_pad == o.P_pad and p.H == o.H
+    assert p.F == o.F.tolist() and p.Hoff == o.Hoff.tolist() and p.S == o.S.tolist() and p.h == o.h.tolist()
+    # every slice starts on a multiple of align in the full and the shard buffers, so every
+    # segment's full and shard positions are aligned alike (no shifted gradient rows)
+    for (g, s, ln, valid, r, u) in Z.zero_plan_segments(p.handle):
+        assert (g - s) % align == 0 and (p.F[u] + r * p.h[u]) % align == 0
+
+
+@pytest.mark.parametrize("align", [1, 8])
 @pytest.mark.parametrize("sizes,N", _units_cases()[:20])
-def test_launch_table_covers_every_slice_once(zlib, orc, sizes, N):
-    p = Z.ZeroPlan(sizes, N)
+def test_launch_table_covers_every_slice_once(zlib, orc, sizes, N, align):
+    p = Z.ZeroPlan(sizes, N, align=align)
     segs = Z.zero_plan_segments(p.handle)
-    o = orc.Plan(sizes, N)
+    o = orc.Plan(sizes, N, align)
     if o.P_pad == 0:
         assert segs == []
         return
@@ -122,6 +137,9 @@ def test_argument_errors_are_reported_on_the_host(zlib):
     assert L.zero_plan_create(sizes, 2, 2, None) == B.ZERO_EINVAL
     huge = (C.c_int64 * 2)(2 ** 62, 2 ** 62)
     assert L.zero_plan_create(huge, 2, 2, C.byref(h)) == B.ZERO_EINVAL
+    assert L.zero_plan_create_aligned(sizes, 2, 2, 0, C.byref(h)) == B.ZERO_EINVAL
+    assert L.zero_plan_create_aligned(sizes, 2, 2, 4097, C.byref(h)) == B.ZERO_EINVAL
+    assert L.zero_plan_align(None, C.byref(C.c_int32())) == B.ZERO_EINVAL
     assert L.zero_plan_create(sizes, 2, 2, C.byref(h)) == B.ZERO_OK
     # device calls on a plan without a workspace fail before any CUDA call
     ptrs = (C.c_void_p * 2)(16, 32)

@@ -109,6 +109,42 @@ def test_finewrap_shaped_small_bit_exact():
         c.assert_full_equal()
 
 
+@pytest.mark.parametrize("align,gd", [(8, W.BF16), (4, W.F32), (2, W.BF16)])
+def test_aligned_plan_steps_bit_exact(align, gd):
+    """Plans with the alignment option (every unit padded to a multiple of N*align):
+    fine-wrap-shaped units at N=16, where an unaligned plan puts most slices at
+    shifted offsets; here no segment is shifted, and the fused and the clipped
+    steps equal the oracle's on the same aligned layout."""
+    sizes = W.finewrap_units(n_units=300, lo_log2=0, hi_log2=14, seed=5)
+    c = SmallCase(sizes, 16, gd, W.BF16, seed=align, align=align, grad_sigma=1e-2, outlier_frac=1e-3,
+                  outlier_scale=100.0)
+    segs = Z.zero_plan_segments(c.plan.handle)
+    assert all((g - s_) % align == 0 for (g, s_, _, _, _, _) in segs)
+    for t, max_norm in ((1, 0.0), (2, 1e-3), (3, 0.0)):
+        c.gpu_step(t, max_norm=max_norm)
+        assert c.oracle_step(t, max_norm=max_norm) == O.OK
+        if max_norm > 0:
+            assert abs(c.sq.item() - c.S_o) <= S_RTOL * c.S_o
+        c.assert_state_equal()
+        c.assert_full_equal()
+        c.assert_pshard_equal()
+
+
+@pytest.mark.parametrize("n_from,a_from,n_to,a_to", [(16, 1, 16, 8), (16, 8, 8, 1), (8, 8, 3, 2)])
+def test_reshard_between_alignments_bit_exact(n_from, a_from, n_to, a_to):
+    sizes = W.finewrap_units(n_units=30, lo_log2=0, hi_log2=15, seed=n_from + a_from) + [1, 70001]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pf, pt = Z.ZeroPlan(sizes, n_from, dev, align=a_from), Z.ZeroPlan(sizes, n_to, dev, align=a_to)
+    g = torch.Generator().manual_seed(n_from * 3 + a_to)
+    src_h = torch.randn(n_from, pf.H, generator=g)
+    src = aligned_copy(src_h, dev)
+    dst = Z.rank_buffers(n_to, pt.H, torch.float32, dev)
+    dst.fill_(7.0)
+    Z.zero_reshard(pf, pt, src, dst)
+    want = O.reshard(sizes, n_from, n_to, host_bits(src_h), align_from=a_from, align_to=a_to)
+    assert np.array_equal(host_bits(dst), want)
+
+
 def test_empty_and_degenerate_plans():
     for sizes, N in (([], 4), ([0, 0], 3), ([1], 64), ([0, 1, 0], 2)):
         c = SmallCase(sizes, N, W.BF16, W.BF16)
@@ -522,6 +558,22 @@ def test_sharded_checkpoint_reshard_then_continue(tmp_path):
     assert c4.oracle_step(2) == O.OK
     c4.assert_state_equal()
     c4.assert_full_equal()
+
+
+def test_checkpoint_between_alignments(tmp_path):
+    """Save from an aligned N=16 plan, load into an unaligned N=8 plan: the reshard at
+    load time maps between the two layouts exactly as the oracle does."""
+    from fsdp_sharded_optimizer_step_gb300 import checkpoint
+    sizes = W.finewrap_units(n_units=25, lo_log2=4, hi_log2=16, seed=8)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pa, pb = Z.ZeroPlan(sizes, 16, dev, align=8), Z.ZeroPlan(sizes, 8, dev)
+    g = torch.Generator().manual_seed(88)
+    arrays = {"master": aligned_copy(torch.randn(16, pa.H, generator=g), dev)}
+    checkpoint.save(str(tmp_path), pa, arrays, step=2)
+    state, step = checkpoint.load(str(tmp_path), pb)
+    assert step == 2
+    want = O.reshard(sizes, 16, 8, host_bits(arrays["master"]), align_from=8, align_to=1)
+    assert np.array_equal(host_bits(state["master"]), want)
 
 
 def test_checkpoint_load_on_a_side_stream(tmp_path):
