@@ -67,6 +67,58 @@ def test_toy_zero2_bit_exact_every_step():
     assert np.array_equal(host_bits(master).ravel(), f32bits(ref))
 
 
+@pytest.mark.slow
+def test_toy_3000_steps_bit_exact():
+    """The pages' toy run for 3000 steps (well past the bias corrections' transient and
+    into Adam's oscillation band around the mean target): the GPU state equals the
+    oracle's after every 100th step, and at the end."""
+    dev = torch.device("cuda")
+    N, P = 4, 1000
+    plan = Z.ZeroPlan(W.toy_units(), N, dev)
+    targets = W.toy_targets(N, P, device=dev)
+    full = torch.zeros(P, dtype=torch.float32, device=dev)
+    master, m, v = (Z.rank_buffers(N, plan.H, torch.float32, dev, zero=True) for _ in range(3))
+    grads = Z.rank_buffers(N, P, torch.float32, dev)
+    t_np = targets.cpu().numpy()
+    w_o, m_o, v_o = (np.zeros(P, np.float32) for _ in range(3))
+    for t in range(1, 3001):
+        torch.sub(full.unsqueeze(0), targets, out=grads)
+        hp, ohp = hp_for(t)
+        Z.zero_step(plan, grads, master, m, v, hp, full=full)
+        O.adamw([w_o - t_np[r] for r in range(N)], O.F32, w_o, m_o, v_o, ohp, pdtype=O.F32)
+        if t % 100 == 0:
+            assert np.array_equal(host_bits(full), f32bits(w_o)), f"step {t}"
+    assert np.array_equal(host_bits(master).ravel(), f32bits(w_o))
+    assert np.array_equal(host_bits(m).ravel(), f32bits(m_o)) and np.array_equal(host_bits(v).ravel(), f32bits(v_o))
+
+
+def test_random_layouts_and_hyperparameters():
+    """A seeded fuzz over unit lists, rank counts, gradient and param dtypes, the alignment
+    option and the AdamW constants (b1, b2, eps, lr, weight decay including 0, step numbers
+    up to 10^6, clipping on and off): every case bit-exact against the oracle."""
+    rng = np.random.default_rng(2026)
+    for case in range(24):
+        U = int(rng.integers(1, 9))
+        sizes = [int(x) for x in rng.integers(0, 40000, U)]
+        N = int(rng.choice([1, 2, 3, 4, 5, 7, 8, 12, 16, 24]))
+        gd, pd = (W.BF16 if rng.random() < 0.7 else W.F32), (W.BF16 if rng.random() < 0.7 else W.F32)
+        align = int(rng.choice([1, 1, 2, 8]))
+        c = SmallCase(sizes, N, gd, pd, seed=case, align=align, grad_sigma=float(10 ** rng.uniform(-5, 0)))
+        over = dict(lr=float(10 ** rng.uniform(-5, -1)), b1=float(rng.choice([0.0, 0.5, 0.9, 0.99])),
+                    b2=float(rng.choice([0.9, 0.95, 0.999, 0.9999])), eps=float(10 ** rng.uniform(-12, -4)),
+                    wd=float(rng.choice([0.0, 0.01, 0.1, 0.5])))
+        t0 = int(rng.choice([1, 2, 10, 1000, 10 ** 6]))
+        for k in range(2):
+            max_norm = float(10 ** rng.uniform(-3, 1)) if rng.random() < 0.4 else 0.0
+            c.gpu_step(t0 + k, max_norm=max_norm, **over)
+            assert c.oracle_step(t0 + k, max_norm=max_norm, **over) == O.OK, case
+            if max_norm > 0:
+                assert abs(c.sq.item() - c.S_o) <= S_RTOL * c.S_o, case
+            c.assert_state_equal()
+            c.assert_full_equal()
+            c.assert_pshard_equal()
+
+
 # ------------------------------------------------------------------ small configs, every element
 SMALL = [
     # (sizes, N, gdtype, pdtype)
