@@ -217,9 +217,11 @@ struct zero_offload {
     // device side, made by the first step on the plan's device
     bool streams_ready = false;
     cudaStream_t d2h = nullptr, h2d = nullptr;
-    cudaEvent_t ev_start = nullptr, ev_landed = nullptr, ev_sent = nullptr;
+    cudaEvent_t ev_start = nullptr, ev_landed = nullptr, ev_sent = nullptr, ev_norm = nullptr;
     std::vector<cudaEvent_t> reduced, landed;
-    double *host_S = nullptr;  // page-locked, for the clip's S
+    // the clip's S, written by the total's kernel straight into mapped page-locked host
+    // memory: a copy would queue on the copy engine behind the gradient shard's copies
+    double *host_S = nullptr, *host_S_dev = nullptr;
     // timings of the last step
     double call_ms = 0, wait_ms = 0, cpu_ms = 0;
     bool stepped = false;
@@ -282,11 +284,12 @@ void release_device_side(zero_offload *eng) {
         if (ev != nullptr) cudaEventDestroy(ev), ev = nullptr;
     for (cudaEvent_t &ev : eng->landed)
         if (ev != nullptr) cudaEventDestroy(ev), ev = nullptr;
-    for (cudaEvent_t *ev : {&eng->ev_start, &eng->ev_landed, &eng->ev_sent})
+    for (cudaEvent_t *ev : {&eng->ev_start, &eng->ev_landed, &eng->ev_sent, &eng->ev_norm})
         if (*ev != nullptr) cudaEventDestroy(*ev), *ev = nullptr;
     for (cudaStream_t *st : {&eng->d2h, &eng->h2d})
         if (*st != nullptr) cudaStreamDestroy(*st), *st = nullptr;
     if (eng->host_S != nullptr) cudaFreeHost(eng->host_S), eng->host_S = nullptr;
+    eng->host_S_dev = nullptr;
     eng->streams_ready = false;
 }
 
@@ -301,7 +304,9 @@ int make_device_side(zero_offload *eng) {
     if (e == cudaSuccess) e = cudaEventCreate(&eng->ev_start);
     if (e == cudaSuccess) e = cudaEventCreate(&eng->ev_landed);
     if (e == cudaSuccess) e = cudaEventCreate(&eng->ev_sent);
-    if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void **>(&eng->host_S), 64, cudaHostAllocDefault);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&eng->ev_norm, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void **>(&eng->host_S), 64, cudaHostAllocMapped);
+    if (e == cudaSuccess) e = cudaHostGetDevicePointer(reinterpret_cast<void **>(&eng->host_S_dev), eng->host_S, 0);
     for (size_t b = 0; e == cudaSuccess && b < eng->batches.size(); ++b) {
         e = cudaEventCreateWithFlags(&eng->reduced[b], cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&eng->landed[b], cudaEventDisableTiming);
@@ -459,15 +464,14 @@ extern "C" int zero_offload_step(zero_offload *eng, const void *const *grads, in
         float coef = 1.0f;
         double S = 0.0;
         if (clip) {
-            // the fixed-order total of every segment's sum of squares, read back once
-            if ((rc = launch_finalize(plan, hp->max_norm, nullptr, st)) != ZERO_OK) return rc;
-            if ((e = cudaMemcpyAsync(eng->host_S, plan->d_sqnorm, sizeof(double), cudaMemcpyDeviceToHost, st)) !=
-                cudaSuccess)
-                return cuda_fail(e);
+            // the fixed-order total of every segment's sum of squares, written to the host directly
+            *reinterpret_cast<volatile double *>(eng->host_S) = std::nan("");
+            if ((rc = launch_finalize(plan, hp->max_norm, eng->host_S_dev, st)) != ZERO_OK) return rc;
+            if ((e = cudaEventRecord(eng->ev_norm, st)) != cudaSuccess) return cuda_fail(e);
             const auto t0 = std::chrono::steady_clock::now();
-            if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e);
+            if ((e = cudaEventSynchronize(eng->ev_norm)) != cudaSuccess) return cuda_fail(e);
             eng->wait_ms += ms_since(t0);
-            S = *eng->host_S;
+            S = *reinterpret_cast<volatile double *>(eng->host_S);
             if (sqnorm_out != nullptr) *sqnorm_out = S;
             if (!std::isfinite(S)) {
                 // skip the update: nothing of the state or the params is touched
