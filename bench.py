@@ -470,6 +470,7 @@ def measure_e2e(args, world, dev, stream, grads, full, step, N, P, gdt, pdt, psi
            # the host link's speed varies from step to step: the per-step spread, and the link rate
            # the fastest step reached (all copied bytes over its time)
            "median_ms": statistics.median(per_step), "min_ms": min(per_step), "max_ms": max(per_step),
+           "per_step_ms": [round(x, 2) for x in per_step],
            "link_GBs_at_min": (h2d + d2h) / (min(per_step) / 1e3) / 1e9,
            "mode": ("streamed per unit: copy-in, norm pass, then update and copy-out overlapped" if max_norm > 0
                     else "streamed per unit: copy-in, update and copy-out overlapped") if streamed

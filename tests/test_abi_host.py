@@ -232,3 +232,23 @@ def test_rank_pointers_of_a_2d_tensor_match_its_rows():
         B._rows(Plan, torch.zeros(3, 10, dtype=torch.bfloat16), 10, "x", B._G)  # wrong rank count
     with pytest.raises(ValueError):
         B._rows(Plan, torch.zeros(4, 10, dtype=torch.float16), 10, "x", B._G)  # dtype
+
+
+def test_committed_profiles_describe_the_current_kernel_source():
+    """Every ncu summary under profiles/ records the hash of the kernel source it was
+    captured from; the bench reports its DRAM traffic only while the hash matches, so a
+    kernel change must come with recaptured summaries."""
+    import glob
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    want = {"kernel": bench.kernel_source_hash(), "reshard": bench.reshard_source_hash()}
+    files = sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md")))
+    assert files
+    for path in files:
+        text = open(path).read()
+        m = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
+        assert m, path
+        kind = "reshard" if os.path.basename(path).startswith("k_reshard") else "kernel"
+        assert m.group(1) == want[kind], f"{os.path.basename(path)} was captured from another kernel source"
+        assert re.search(r"dram_bytes_per_launch:\s*[0-9]+", text), path
