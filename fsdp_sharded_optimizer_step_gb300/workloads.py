@@ -91,6 +91,13 @@ CONFIGS = {
                             "bf16 grads N(0,1e-3); about 3.6 GB resident",
                        units=lambda: llm_4b_units()[:1], N=8, gdtype=BF16, pdtype=BF16, stage=3, steps=3,
                        max_norm=0.0, grad_sigma=1e-3, master_sigma=0.02),
+    "beyond_2p32": dict(desc="index-width case: N=2, units of 2^31+3, 7, 2^31+2^24+5 and 1 elements "
+                             "(4,311,744,532 padded positions: full positions beyond 2^32, shard positions "
+                             "beyond 2^31), bf16 grads N(0,1e-2) with 0.1% outliers x100, clip 1.0; "
+                             "about 103 GB resident with the ZeRO-3 param shards",
+                        units=lambda: [2 ** 31 + 3, 7, 2 ** 31 + 2 ** 24 + 5, 1], N=2, gdtype=BF16, pdtype=BF16,
+                        stage=2, steps=2, max_norm=1.0, grad_sigma=1e-2, outlier_frac=1e-3, outlier_scale=100.0,
+                        master_sigma=0.02),
     "4b_z3": dict(desc="4B ZeRO-3: N=8, 33 units, bf16 grads N(0,1e-3), per-unit bf16 all-gather",
                   units=llm_4b_units, N=8, gdtype=BF16, pdtype=BF16, stage=3, steps=3, max_norm=0.0,
                   grad_sigma=1e-3, master_sigma=0.02),

@@ -7,6 +7,9 @@ compare a seeded sample of positions the oracle can follow one by one (the
 update is element-wise, so each sampled position depends only on its own
 gradients, state and the global clip coefficient).
 """
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -201,12 +204,13 @@ class SmallCase:
         assert bad.size == 0, f"pshard: {bad.shape[0]} differ, first at {bad[0]}"
 
 
-def sample_positions(plan_o: "O.Plan", n_random, seed, extra_units=()):
+def sample_positions(plan_o: "O.Plan", n_random, seed, extra_units=(), extra_pos=()):
     """Seeded random full positions plus every unit's first/last element, every
-    slice boundary and ragged tail, and all positions of the units in extra_units."""
+    slice boundary and ragged tail, the given extra positions, and all positions
+    of the units in extra_units."""
     rng = np.random.default_rng(seed)
     P = plan_o.P_pad
-    pos = [rng.integers(0, P, n_random)]
+    pos = [rng.integers(0, P, n_random), np.asarray(extra_pos, np.int64)]
     N = plan_o.N
     for u in range(len(plan_o.sizes)):
         F, S, h = int(plan_o.F[u]), int(plan_o.S[u]), int(plan_o.h[u])
@@ -231,7 +235,7 @@ def sample_positions(plan_o: "O.Plan", n_random, seed, extra_units=()):
 class SampledCase:
     """A full-size config: GPU runs everything, the oracle follows a sample."""
 
-    def __init__(self, name, n_random=200000, seed=0, device="cuda", extra_units=(), stage=None):
+    def __init__(self, name, n_random=200000, seed=0, device="cuda", extra_units=(), stage=None, extra_pos=()):
         cfg = W.CONFIGS[name]
         self.cfg = cfg
         self.sizes = cfg["units"]()
@@ -255,7 +259,7 @@ class SampledCase:
         self.gshard = Z.rank_buffers(N, H, torch.float32, self.device) if self.clip else None
         self.sq = torch.zeros(1, dtype=torch.float64, device=self.device)
         # the sample
-        self.pos = sample_positions(self.o, n_random, seed, extra_units)
+        self.pos = sample_positions(self.o, n_random, seed, extra_units, extra_pos)
         self.rank, self.spos, self.padflag = self.o.locate(self.pos)
         pos_t = torch.from_numpy(self.pos).to(self.device)
         self.g_s = oracle_grad_rows(self.grads.index_select(1, pos_t))
@@ -267,15 +271,24 @@ class SampledCase:
         self.pos_t = pos_t
         self.S_o = None
 
-    def oracle_sqnorm(self, chunk=1 << 26):
-        """Exact S over every position (streamed through host memory in chunks)."""
-        acc = O.SqAcc()
+    def oracle_sqnorm(self, chunk=1 << 25, threads=8):
+        """Exact S over every position, streamed through host memory in chunks on a
+        few host threads, each with its own exact accumulator; exact sums merge
+        exactly, so the split does not change the result."""
         pad = self.o.pad_mask()
         P = self.plan.P_pad
-        for a in range(0, P, chunk):
+
+        def part(a):
+            acc = O.SqAcc()
             b = min(P, a + chunk)
             acc.add_avg_grad(oracle_grad_rows(self.grads[:, a:b]), ODT[self.gdtype], pad[a:b])
-        self.S_o = acc.result()
+            return acc
+
+        total = O.SqAcc()
+        with ThreadPoolExecutor(max(1, min(threads, os.cpu_count() or 1))) as ex:
+            for acc in ex.map(part, range(0, P, chunk)):
+                total.merge(acc)
+        self.S_o = total.result()
         return self.S_o
 
     def gpu_step(self, t):

@@ -117,6 +117,25 @@ def test_named_workloads_layout(zlib, orc):
         assert Z.zero_plan_workspace_bytes(p.handle) >= 40 * p.n_segments
 
 
+def test_index_width_workload_layout(zlib, orc):
+    """The index-width workload's plan passes 2^32 full positions and 2^31 shard
+    positions, and its launch table still covers every position once, each segment
+    at the same offset into its slice in both index spaces."""
+    sizes = W.CONFIGS["beyond_2p32"]["units"]()
+    p = Z.ZeroPlan(sizes, 2)
+    o = orc.Plan(sizes, 2)
+    assert p.P_pad == o.P_pad > 2 ** 32 and p.H == o.H > 2 ** 31
+    assert p.F == o.F.tolist() and p.Hoff == o.Hoff.tolist() and p.h == o.h.tolist()
+    seg = np.array(Z.zero_plan_segments(p.handle), dtype=np.int64)
+    g, s, ln, valid, r, u = seg.T
+    F, Hoff, h = (np.array(x, np.int64) for x in (p.F, p.Hoff, p.h))
+    assert ln.sum() == p.P_pad and (g + ln).max() == p.P_pad
+    assert np.array_equal(g - F[u] - r * h[u], s - Hoff[u])
+    order = np.argsort(g, kind="stable")
+    assert np.array_equal(g[order][1:], (g + ln)[order][:-1])  # contiguous, no overlap
+    assert (s + ln).max() == p.H
+
+
 def test_bias_corrections_match_oracle_bitwise(zlib, orc):
     for b1, b2 in [(0.9, 0.95), (0.9, 0.999), (0.8, 0.99), (0.5, 0.5)]:
         for t in list(range(1, 3000)) + [10000, 123457, 2 ** 31 - 1]:

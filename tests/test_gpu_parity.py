@@ -215,8 +215,12 @@ def test_pads_stay_zero():
     mp = torch.from_numpy(c.map)
     padpos = pad[mp].to(c.device)  # [N, H] mask of padding shard positions
     c.master[padpos] = 0.0
+    c.reload()
     for t in (1, 2, 3, 4):
         c.gpu_step(t)
+        assert c.oracle_step(t) == O.OK
+        c.assert_state_equal()
+        c.assert_full_equal()
     assert torch.all(c.master[padpos] == 0) and torch.all(c.m[padpos] == 0) and torch.all(c.v[padpos] == 0)
     assert torch.all(c.full[torch.from_numpy(c.pad.astype(bool)).to(c.device)].float() == 0)
 
@@ -567,6 +571,54 @@ def test_4b_zero3_full_size_sampled():
     c = SampledCase("4b_z3", n_random=300000, extra_units=(0, 1, 16, 31))
     c.gpu_step(1)
     c.assert_sample_equal(c.oracle_step(1))
+
+
+def _index_width_positions(o):
+    """Full positions on either side of 2^31 and 2^32, the last one, and for every rank the
+    full positions whose shard positions sit on either side of 2^31."""
+    P, N = o.P_pad, o.N
+    pos = [p for b in (2 ** 31, 2 ** 32) for p in (b - 2, b - 1, b, b + 1) if 0 <= p < P] + [P - 1]
+    hoff = np.concatenate([[0], np.cumsum(o.h)])
+    for s in (2 ** 31 - 2, 2 ** 31 - 1, 2 ** 31, 2 ** 31 + 1):
+        u = int(np.searchsorted(hoff, s, side="right")) - 1
+        if u < len(o.sizes) and s < hoff[u + 1]:
+            pos += [int(o.F[u]) + r * int(o.h[u]) + int(s - hoff[u]) for r in range(N)]
+    return pos
+
+
+@pytest.mark.slow
+def test_beyond_2p32_positions_clipped_then_zero3():
+    """Index width: 4,311,744,532 padded positions at N=2, two units longer than 2^31,
+    so full positions pass 2^32 and shard positions (8.6 GB into each fp32 rank buffer)
+    pass 2^31.  Step 1 is the clipped step (S over every position within the norm
+    bound of the oracle's exact sum, the coefficient bit-exact), step 2 the unclipped
+    step with bf16 param shards and per-unit gathers (ZeRO-3); both against the oracle
+    on 200k random positions, every slice boundary and the positions either side of
+    2^31 and 2^32 in both index spaces."""
+    o = O.Plan(W.CONFIGS["beyond_2p32"]["units"](), 2)
+    extra = _index_width_positions(o)
+    assert max(extra) >= 2 ** 32 and len(extra) >= 9 + 4 * 2
+    c = SampledCase("beyond_2p32", n_random=200000, stage=3, extra_pos=extra)
+    assert c.plan.P_pad > 2 ** 32 and c.plan.H > 2 ** 31
+    S = c.oracle_sqnorm()
+    coef = O.clip_coef(S, 1.0)
+    assert coef < 1.0
+    hp, _ = hp_for(1, 1.0)
+    Z.zero_step(c.plan, c.grads, c.master, c.m, c.v, hp, full=c.full, pshard=c.pshard, gshard_ws=c.gshard,
+                sqnorm_out=c.sq)
+    S_gpu = c.sq.item()
+    assert abs(S_gpu - S) <= S_RTOL * S
+    assert O.clip_coef(S_gpu, 1.0) == coef
+    c.assert_sample_equal(c.oracle_step(1, coef=coef))
+    assert Z.zero_plan_check(c.plan) == 0
+    c.full.zero_()
+    c.clip = False
+    hp, _ = hp_for(2)
+    Z.zero_step(c.plan, c.grads, c.master, c.m, c.v, hp, full=None, pshard=c.pshard)
+    for u in range(c.plan.n_units):  # ZeRO-3: the param shards gathered unit by unit
+        Z.zero_all_gather_bf16(c.plan, c.pshard, c.full, unit=u)
+    c.assert_sample_equal(c.oracle_step(2))
+    assert Z.zero_plan_check(c.plan) == 0
 
 
 # ------------------------------------------------------------------ checkpoint resharding
