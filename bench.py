@@ -337,7 +337,7 @@ def update_bytes_per_element(cfg):
 E2E_PINNED_BUDGET = 32e9
 
 
-SECONDARY = ("4b_z3", "1p3b_clip", "finewrap")
+SECONDARY = ("4b_z3", "1p3b_clip", "finewrap", "finewrap600")
 
 
 def run_secondary(name, steps, warmup, dev):
@@ -409,12 +409,55 @@ def run_secondary(name, steps, warmup, dev):
                       "roofline": {"bound": "hbm", "achieved": upd_gbs, "peak": peak, "unit": "GB/s",
                                    "frac": upd_gbs / peak, "traffic": traffic, "peak_kind": peak_kind}},
            "clocks": clock_info}
+    if name.startswith("finewrap"):
+        out["per_unit"] = per_unit_timing(plan, grads, master, m, v, full, steps, warmup, dev, stream, upd_ms)
     step_bpe = bpe + (4 if z3 else 0)  # ZeRO-3: + the per-unit gathers (2 B read + 2 B written per element)
     step_gbs = step_bpe * P / (ms / 1e3) / 1e9
     out["step_roofline"] = {"bound": "hbm", "achieved": step_gbs, "peak": peak, "unit": "GB/s", "frac": step_gbs / peak,
                             "pct_of_8tbs_nominal": 100 * step_gbs / 8000.0, "bytes_per_element": step_bpe,
                             "peak_kind": peak_kind}
     return out
+
+
+def per_unit_timing(plan, grads, master, m, v, full, steps, warmup, dev, stream, one_launch_ms):
+    """The same unclipped step as one launch per unit instead of the one multi-unit launch:
+    launched from Python once, then captured in a CUDA graph and replayed (t fixed at
+    capture), each timed with CUDA events on the launching stream."""
+    import fsdp_sharded_optimizer_step_gb300 as Z
+    from fsdp_sharded_optimizer_step_gb300 import workloads as W
+
+    def unit_step(t):
+        hp = Z.AdamW(t=t, **W.HP)
+        for u in range(plan.n_units):
+            Z.zero_step(plan, grads, master, m, v, hp, full=full, unit=u)
+
+    def timed(fn, reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / reps
+
+    t = 1000
+    unit_step(t)
+    torch.cuda.synchronize(dev)
+    python_ms = timed(lambda: unit_step(t), 1)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.graph(graph, stream=cap, capture_error_mode="relaxed"):
+        unit_step(t)
+    stream.wait_stream(cap)
+    torch.cuda.synchronize(dev)
+    for _ in range(warmup):
+        graph.replay()
+    graph_ms = timed(graph.replay, steps)
+    del graph
+    return {"launches_per_step": plan.n_units, "ms_launched_from_python": python_ms,
+            "ms_replayed_from_cuda_graph": graph_ms, "one_launch_ms": one_launch_ms,
+            "graph_vs_one_launch": graph_ms / one_launch_ms}
 
 
 def measure_e2e(args, world, dev, stream, grads, full, step, N, P, gdt, pdt, psi, plan=None, state=None, streamed=False,

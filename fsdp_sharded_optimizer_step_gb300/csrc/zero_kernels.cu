@@ -41,6 +41,21 @@ __host__ __device__ constexpr int consumer_warps() {
 static_assert(consumer_warps<16>() <= kPartialSlots && consumer_warps<8>() <= kPartialSlots,
               "one partial slot per consumer warp");
 
+// k_pipe in FUSED and SHARD mode has one more warp, the edge warp: it updates
+// each segment's head and tail elements (before the shard position reaches a
+// multiple of 8, after the last 8-group) with direct loads while the consumer
+// warps stream the body, so the latency of those loads no longer holds up the
+// ring.  REDUCE mode keeps them in the consumer warps, whose partial sums of
+// squares they belong to.
+template <int MODE>
+__host__ __device__ constexpr int edge_warps() {
+    return MODE == MODE_REDUCE ? 0 : 1;
+}
+template <int MODE, int NR>
+__host__ __device__ constexpr int pipe_threads() {
+    return (consumer_warps<NR>() + 1 + edge_warps<MODE>()) * 32;
+}
+
 // Diagnostic build (-DZERO_SELFCHECK): every shared/global access of the
 // pipeline is checked against its buffer and alignment first; a failed check
 // records its code in *err and the access is skipped.
@@ -334,7 +349,7 @@ __device__ __forceinline__ SqPartial warp_sq(const SqAcc &a) {
 // the host coefficient; SHARD: the device clip coefficient).
 template <int MODE, int GD, int NR>
 __device__ __forceinline__ void direct_segment(const KParams &p, const Seg &sg, const SegSplit &sp, int tid, int nthr,
-                                               bool body, bool scale, float coef, SqAcc &sq) {
+                                               bool body, bool edges, bool scale, float coef, SqAcc &sq) {
     const int r = sg.rank;
     float *__restrict__ W = p.master[r] + sg.s_off;
     float *__restrict__ M = p.m[r] + sg.s_off;
@@ -381,7 +396,7 @@ __device__ __forceinline__ void direct_segment(const KParams &p, const Seg &sg, 
             }
         }
     }
-    const int nedge = sp.k0 + (sg.len - sp.tail0);
+    const int nedge = edges ? sp.k0 + (sg.len - sp.tail0) : 0;
     for (int t = tid; t < nedge; t += nthr) {
         const int k = t < sp.k0 ? t : sp.tail0 + (t - sp.k0);
         if (!ZERO_GUARD(k >= 0 && k < sg.len && sg.s_off + k < p.h_len && sg.g_off + k < p.p_pad &&
@@ -642,9 +657,28 @@ __device__ __forceinline__ bool pipe_eligible(const KParams &p, const Seg &sg, c
     return end_bytes <= limit;
 }
 
+// A segment descriptor handed through shared memory (volatile: the ring's
+// mbarriers order these accesses, the compiler must not move them).
+__device__ __forceinline__ void put_seg(Seg *dst, const Seg &sg) {
+    volatile int64_t *d = reinterpret_cast<volatile int64_t *>(dst);
+    const int64_t *s = reinterpret_cast<const int64_t *>(&sg);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = s[i];
+}
+
+__device__ __forceinline__ Seg get_seg(const Seg *src) {
+    Seg sg;
+    const volatile int64_t *s = reinterpret_cast<const volatile int64_t *>(src);
+    int64_t *d = reinterpret_cast<int64_t *>(&sg);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = s[i];
+    return sg;
+}
+
 template <int MODE, int GD, int NR>
-__global__ void __launch_bounds__((consumer_warps<NR>() + 1) * 32, 1) k_pipe(const KParams p, int64_t nseg) {
+__global__ void __launch_bounds__(pipe_threads<MODE, NR>(), 1) k_pipe(const KParams p, int64_t nseg) {
     constexpr int CW = consumer_warps<NR>();
+    constexpr int EW = edge_warps<MODE>();
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int GB = GD == ZERO_BF16 ? 2 : 4;  // bytes per gradient element
     constexpr int SHIFT_MASK = 16 / GB - 1;      // elements per 16 bytes, minus one
@@ -663,9 +697,10 @@ __global__ void __launch_bounds__((consumer_warps<NR>() + 1) * 32, 1) k_pipe(con
     uint64_t *empty_bar = full_bar + stages;
     __shared__ int abort_flag;
     // segment ring: the producer publishes each segment number it took (-1: no more) in
-    // seg_ring[slot] and arrives on seg_full[slot]; every consumer warp arrives on
-    // seg_empty[slot] once it has read the number
+    // seg_ring[slot], its descriptor in seg_data[slot], and arrives on seg_full[slot]; every
+    // consumer warp (and the edge warp) arrives on seg_empty[slot] once it has read them
     __shared__ int64_t seg_ring[kSegRing];
+    __shared__ Seg seg_data[kSegRing];
     __shared__ __align__(8) uint64_t seg_full[kSegRing], seg_empty[kSegRing];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -675,7 +710,7 @@ __global__ void __launch_bounds__((consumer_warps<NR>() + 1) * 32, 1) k_pipe(con
         }
         for (int s = 0; s < kSegRing; ++s) {
             mbar_init(&seg_full[s], 1);
-            mbar_init(&seg_empty[s], CW);
+            mbar_init(&seg_empty[s], CW + EW);
         }
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -697,10 +732,13 @@ __global__ void __launch_bounds__((consumer_warps<NR>() + 1) * 32, 1) k_pipe(con
         for (;;) {
             const unsigned long long t = next_ticket;
             const int64_t si = ok && t < static_cast<unsigned long long>(nseg) ? static_cast<int64_t>(t) : -1;
+            Seg sg{};
+            if (si >= 0) sg = p.segs[p.seg_base + si];
             if (!mbar_wait(&seg_empty[rs], rphase ^ 1u)) {  // the consumers stopped taking segments
                 ok = false;
                 break;
             }
+            put_seg(&seg_data[rs], sg);
             *reinterpret_cast<volatile int64_t *>(&seg_ring[rs]) = si;
             mbar_arrive(&seg_full[rs]);  // release: the number is visible to the warps that see the phase
             if (++rs == kSegRing) {
@@ -710,7 +748,6 @@ __global__ void __launch_bounds__((consumer_warps<NR>() + 1) * 32, 1) k_pipe(con
             if (si < 0) break;
             next_ticket = atomicAdd(&p.tickets[0], 1ull);
             int64_t tile_no = 0;  // position of the tile in its segment
-            const Seg sg = p.segs[p.seg_base + si];
             const SegSplit sp = split_segment(sg, p.g_origin);
             if (!pipe_eligible<MODE, GB>(p, sg, sp)) continue;
             const int r = sg.rank;
@@ -784,6 +821,34 @@ __global__ void __launch_bounds__((consumer_warps<NR>() + 1) * 32, 1) k_pipe(con
         return;
     }
 
+    if (EW > 0 && warp == CW + 1) {
+        // ---------------- edge warp: the heads and tails of the segments, in ring order
+        int rs = 0;
+        uint32_t rphase = 0;
+        SqAcc sq;  // no sums of squares in these modes
+        sq_reset(sq);
+        for (;;) {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&seg_full[rs], rphase))) {  // no segment number in time
+                if (lane == 0) atomicExch(p.err, 3);
+                abort_flag = 1;
+                break;
+            }
+            const int64_t si = *reinterpret_cast<volatile int64_t *>(&seg_ring[rs]);
+            const Seg sg = get_seg(&seg_data[rs]);
+            const int slot = rs;
+            if (++rs == kSegRing) {
+                rs = 0;
+                rphase ^= 1u;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&seg_empty[slot]);
+            if (si < 0) break;
+            const SegSplit sp = split_segment(sg, p.g_origin);
+            direct_segment<MODE, GD, NR>(p, sg, sp, lane, 32, false, true, scale, coef, sq);
+        }
+        return;
+    }
+
     // ---------------- consumers: every consumer warp takes every tile, so each
     // stage's mbarrier phases are always waited on in order by the same warps
     // (a stage shared between consumer sets that alternate would let a waiter
@@ -804,6 +869,7 @@ __global__ void __launch_bounds__((consumer_warps<NR>() + 1) * 32, 1) k_pipe(con
             break;
         }
         const int64_t si = *reinterpret_cast<volatile int64_t *>(&seg_ring[rs]);
+        const Seg sg = get_seg(&seg_data[rs]);
         const int slot = rs;
         if (++rs == kSegRing) {
             rs = 0;
@@ -812,12 +878,11 @@ __global__ void __launch_bounds__((consumer_warps<NR>() + 1) * 32, 1) k_pipe(con
         __syncwarp();
         if (lane == 0) mbar_arrive(&seg_empty[slot]);
         if (si < 0) break;
-        const Seg sg = p.segs[p.seg_base + si];
         const SegSplit sp = split_segment(sg, p.g_origin);
         const bool piped = pipe_eligible<MODE, GB>(p, sg, sp);
         SqAcc sq;
         sq_reset(sq);
-        direct_segment<MODE, GD, NR>(p, sg, sp, ct, CT, !piped, scale, coef, sq);
+        if (!piped || EW == 0) direct_segment<MODE, GD, NR>(p, sg, sp, ct, CT, !piped, EW == 0, scale, coef, sq);
         if (piped && !dead) {
             const int r = sg.rank;
             const int shift = MODE == MODE_SHARD ? 0 : static_cast<int>((sg.g_off - p.g_origin + sp.k0) & SHIFT_MASK);
@@ -1094,7 +1159,7 @@ static int launch_pipe_one(int64_t nseg, KParams &kp, cudaStream_t st) {
     const int rc = sm_count_current_device(&sms);
     if (rc != ZERO_OK) return rc;
     const int64_t grid = nseg < sms ? nseg : sms;
-    k_pipe<MODE, GD, NR><<<static_cast<unsigned>(grid), (CW + 1) * 32, g.smem, st>>>(kp, nseg);
+    k_pipe<MODE, GD, NR><<<static_cast<unsigned>(grid), pipe_threads<MODE, NR>(), g.smem, st>>>(kp, nseg);
     return launch_status();
 }
 

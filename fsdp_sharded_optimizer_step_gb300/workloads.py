@@ -75,6 +75,10 @@ CONFIGS = {
     "finewrap": dict(desc="fine-wrap stress: N=16, 4096 log-uniform units in [2^10, 2^22), bf16 grads N(0,1e-3)",
                      units=finewrap_units, N=16, gdtype=BF16, pdtype=BF16, stage=2, steps=3, max_norm=0.0,
                      grad_sigma=1e-3, master_sigma=0.02),
+    "finewrap600": dict(desc="fine-wrap stress at the stated ~600M total: N=16, 4096 log-uniform units in "
+                             "[2^10, 2^20) (same seed), Psi=638,561,671, bf16 grads N(0,1e-3)",
+                        units=lambda: finewrap_units(hi_log2=20), N=16, gdtype=BF16, pdtype=BF16, stage=2, steps=3,
+                        max_norm=0.0, grad_sigma=1e-3, master_sigma=0.02),
     "gpt2l_prof": dict(desc="profiling case: the first two GPT-2-Large units (token embedding + one block, "
                             "84,006,400 params), N=8, bf16 grads N(0,1e-3); 3.5 GB of traffic per step",
                        units=lambda: gpt2l_units()[:2], N=8, gdtype=BF16, pdtype=BF16, stage=1, steps=3, max_norm=0.0,
@@ -87,6 +91,10 @@ CONFIGS = {
                                "N(0,1e-3); about 3 GB resident",
                           units=lambda: finewrap_units(n_units=128), N=16, gdtype=BF16, pdtype=BF16, stage=2, steps=3,
                           max_norm=0.0, grad_sigma=1e-3, master_sigma=0.02),
+    "finewrap600_prof": dict(desc="profiling case: the first 512 units of finewrap600 (same law and seed, "
+                                  "88,946,467 params), N=16, bf16 grads N(0,1e-3); about 4 GB resident",
+                             units=lambda: finewrap_units(n_units=512, hi_log2=20), N=16, gdtype=BF16, pdtype=BF16,
+                             stage=2, steps=3, max_norm=0.0, grad_sigma=1e-3, master_sigma=0.02),
     "4b_z3_prof": dict(desc="profiling case: one 4B block (d=3072, ffn=8192: 113,252,352 params), N=8, ZeRO-3, "
                             "bf16 grads N(0,1e-3); about 3.6 GB resident",
                        units=lambda: llm_4b_units()[:1], N=8, gdtype=BF16, pdtype=BF16, stage=3, steps=3,

@@ -108,7 +108,8 @@ def test_launch_table_covers_every_slice_once(zlib, orc, sizes, N, align):
 
 
 def test_named_workloads_layout(zlib, orc):
-    for fn, N in [(W.gpt2l_units, 8), (W.gpt_1p3b_units, 8), (W.llm_4b_units, 8), (W.finewrap_units, 16)]:
+    for fn, N in [(W.gpt2l_units, 8), (W.gpt_1p3b_units, 8), (W.llm_4b_units, 8), (W.finewrap_units, 16),
+                  (W.CONFIGS["finewrap600"]["units"], 16)]:
         sizes = fn()
         p = Z.ZeroPlan(sizes, N)
         o = orc.Plan(sizes, N)

@@ -564,6 +564,21 @@ def test_finewrap_full_size_sampled():
 
 
 @pytest.mark.slow
+def test_finewrap600_one_launch_then_per_unit_full_size_sampled():
+    """The fine-wrap law at the stated ~600M total (4096 units in [2^10, 2^20), N=16):
+    step 1 as the one multi-unit launch, step 2 as one launch per unit, each against the
+    oracle on 200k random positions, every slice boundary and four whole units."""
+    c = SampledCase("finewrap600", n_random=200000, extra_units=(0, 1, 2048, 4095))
+    c.gpu_step(1)
+    c.assert_sample_equal(c.oracle_step(1))
+    hp, _ = hp_for(2)
+    for u in range(c.plan.n_units):
+        Z.zero_step(c.plan, c.grads, c.master, c.m, c.v, hp, full=c.full, unit=u)
+    c.assert_sample_equal(c.oracle_step(2))
+    assert Z.zero_plan_check(c.plan) == 0
+
+
+@pytest.mark.slow
 def test_4b_zero3_full_size_sampled():
     """4B ZeRO-3 (128 GB resident): 300k random positions, every slice boundary, and
     every element of four whole 113M-parameter block units (first, second, a middle
