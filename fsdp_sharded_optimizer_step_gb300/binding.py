@@ -77,6 +77,7 @@ def lib():
             "zero_plan_query": (C.c_int, [p, p, p, p, p, p, p]),
             "zero_plan_counts": (C.c_int, [p, p, p, p]),
             "zero_plan_segments": (C.c_int, [p, p]),
+            "zero_plan_local_segments": (C.c_int, [p, C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
             "zero_plan_workspace_bytes": (C.c_int, [p, C.POINTER(C.c_size_t)]),
             "zero_plan_attach": (C.c_int, [p, p, C.c_size_t, p]),
             "zero_bias_corrections": (C.c_int, [i32, f32, f32, p, p]),
@@ -178,6 +179,15 @@ def zero_plan_segments(handle):
     out = (C.c_int64 * max(6 * nseg, 1))()
     _check(lib().zero_plan_segments(handle, out), "zero_plan_segments")
     return [tuple(out[6 * i:6 * i + 6]) for i in range(nseg)]
+
+
+def zero_plan_local_segments(handle):
+    """Unit-local launch table, in the layout of zero_plan_segments."""
+    n = C.c_int64()
+    _check(lib().zero_plan_local_segments(handle, C.byref(n), None), "zero_plan_local_segments")
+    out = (C.c_int64 * max(6 * n.value, 1))()
+    _check(lib().zero_plan_local_segments(handle, C.byref(n), out), "zero_plan_local_segments")
+    return [tuple(out[6 * i:6 * i + 6]) for i in range(n.value)]
 
 
 def zero_plan_workspace_bytes(handle):

@@ -75,6 +75,19 @@ static int seg_range(const zero_plan *plan, int32_t unit, int64_t &begin, int64_
     return ZERO_OK;
 }
 
+// Launches over units [u0, u1) without per-segment partial sums take the
+// unit-local table (each unit cut into about kLocalSegsPerUnit segments, so a
+// small unit still spreads over every SM); whole-plan launches and the norm's
+// passes, whose partials sit at main-table positions, take the main table.
+static int use_local_table(const zero_plan *plan, int32_t u0, int32_t u1, KParams &kp, int64_t &count) {
+    const int64_t begin = plan->unit_local_begin[u0];
+    count = plan->unit_local_begin[u1] - begin;
+    if (count > 0x7FFFFFFF) return ZERO_EINVAL;
+    kp.segs = plan->d_segs_local;
+    kp.seg_base = begin;
+    return ZERO_OK;
+}
+
 static bool valid_dtype(int32_t d) { return d == ZERO_BF16 || d == ZERO_F32; }
 
 int reduce_units(const zero_plan *plan, int32_t u0, int32_t u1, const void *const *grads, int32_t gdtype,
@@ -116,6 +129,12 @@ extern "C" int zero_plan_attach(zero_plan *plan, void *workspace, size_t bytes, 
         if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
     }
     plan->d_segs = reinterpret_cast<Seg *>(base + L.segs);
+    if (!plan->segs_local.empty()) {
+        e = cudaMemcpyAsync(base + L.segs_local, plan->segs_local.data(), plan->segs_local.size() * sizeof(Seg),
+                            cudaMemcpyHostToDevice, reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) { set_last_cuda_error(static_cast<int>(e)); return ZERO_ECUDA; }
+    }
+    plan->d_segs_local = reinterpret_cast<Seg *>(base + L.segs_local);
     plan->d_partials = reinterpret_cast<SqPartial *>(base + L.partials);
     plan->d_sqnorm = reinterpret_cast<double *>(base + L.scalars);
     plan->d_coef = reinterpret_cast<float *>(base + L.scalars + 8);
@@ -237,6 +256,7 @@ extern "C" int zero_all_gather(const zero_plan *plan, const void *const *shard, 
     KParams kp;
     fill_common(plan, kp);
     kp.seg_base = begin;
+    if (unit >= 0 && (rc = use_local_table(plan, unit, unit + 1, kp, count)) != ZERO_OK) return rc;
     kp.pdtype = pdtype;
     kp.full = full;
     for (int q = 0; q < plan->n_ranks; ++q) kp.pshard[q] = const_cast<void *>(shard[q]);
@@ -258,7 +278,7 @@ extern "C" int zero_all_gather_unit(const zero_plan *plan, int32_t unit, const v
     if (!aligned16(dst_unit)) return ZERO_EALIGN;
     KParams kp;
     fill_common(plan, kp);
-    kp.seg_base = begin;
+    if ((rc = use_local_table(plan, unit, unit + 1, kp, count)) != ZERO_OK) return rc;
     kp.pdtype = pdtype;
     kp.full = dst_unit;
     kp.g_origin = plan->F[unit];
@@ -297,6 +317,7 @@ extern "C" int zero_step(const zero_plan *plan, const void *const *grads, int32_
     if (!clip) {
         for (int q = 0; q < n; ++q) kp.grads[q] = grads[q];
         kp.seg_base = begin;
+        if (unit >= 0 && (rc = use_local_table(plan, unit, unit + 1, kp, count)) != ZERO_OK) return rc;
         return launch_pipe(MODE_FUSED, gdtype, count, kp, st);
     }
     // clipped: norm pass (writes the averaged gradient shard), device
@@ -311,11 +332,11 @@ extern "C" int zero_step(const zero_plan *plan, const void *const *grads, int32_
 // Bucket-local variants: grads_b[q] holds only the padded gradient positions
 // of units [u0, u1), element i = full position F_u0 + i (one unit: u1 = u0 + 1).
 static int units_common(const zero_plan *plan, int32_t u0, int32_t u1, const void *const *grads_b, int32_t gdtype,
-                        int64_t &begin, int64_t &count, KParams &kp) {
+                        bool local, int64_t &count, KParams &kp) {
     int rc = check_attached(plan);
     if (rc != ZERO_OK) return rc;
     if (!valid_dtype(gdtype) || u0 < 0 || u1 <= u0 || u1 > plan->n_units) return ZERO_EINVAL;
-    begin = plan->unit_seg_begin[u0];
+    const int64_t begin = plan->unit_seg_begin[u0];
     count = plan->unit_seg_begin[u1] - begin;
     if (count > 0x7FFFFFFF) return ZERO_EINVAL;
     const int64_t f_end = u1 < plan->n_units ? plan->F[u1] : plan->p_pad;
@@ -323,6 +344,7 @@ static int units_common(const zero_plan *plan, int32_t u0, int32_t u1, const voi
     kp.g_origin = plan->F[u0];
     kp.g_len = f_end - plan->F[u0];
     kp.seg_base = begin;
+    if (local && (rc = use_local_table(plan, u0, u1, kp, count)) != ZERO_OK) return rc;
     if (kp.g_len == 0) return ZERO_OK;
     if (grads_b == nullptr) return ZERO_EINVAL;
     for (int q = 0; q < plan->n_ranks; ++q) {
@@ -334,10 +356,10 @@ static int units_common(const zero_plan *plan, int32_t u0, int32_t u1, const voi
 }
 
 static int unit_common(const zero_plan *plan, int32_t unit, const void *const *grads_unit, int32_t gdtype,
-                       int64_t &begin, int64_t &count, KParams &kp) {
+                       bool local, int64_t &count, KParams &kp) {
     if (plan == nullptr) return ZERO_EINVAL;
     if (unit < 0 || unit >= plan->n_units) return ZERO_EINVAL;
-    return units_common(plan, unit, unit + 1, grads_unit, gdtype, begin, count, kp);
+    return units_common(plan, unit, unit + 1, grads_unit, gdtype, local, count, kp);
 }
 
 extern "C" int zero_step_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit, int32_t gdtype,
@@ -345,9 +367,9 @@ extern "C" int zero_step_unit(const zero_plan *plan, int32_t unit, const void *c
                               int32_t pdtype, const zero_hparams *hp, zero_stream_t stream) {
     ZERO_NVTX_RANGE();
     if (hp == nullptr || hp->max_norm > 0.0f) return ZERO_EINVAL;  // a global clip needs every unit
-    int64_t begin = 0, count = 0;
+    int64_t count = 0;
     KParams kp;
-    int rc = unit_common(plan, unit, grads_unit, gdtype, begin, count, kp);
+    int rc = unit_common(plan, unit, grads_unit, gdtype, true, count, kp);
     if (rc != ZERO_OK || count == 0) return rc;
     if ((rc = fill_state(plan, kp, master, m, v, pshard, full, pdtype, hp)) != ZERO_OK) return rc;
     return launch_pipe(MODE_FUSED, gdtype, count, kp, reinterpret_cast<cudaStream_t>(stream));
@@ -358,9 +380,9 @@ extern "C" int zero_step_units(const zero_plan *plan, int32_t u0, int32_t u1, co
                                void *const *pshard, int32_t pdtype, const zero_hparams *hp, zero_stream_t stream) {
     ZERO_NVTX_RANGE();
     if (hp == nullptr || hp->max_norm > 0.0f) return ZERO_EINVAL;  // a global clip needs every unit
-    int64_t begin = 0, count = 0;
+    int64_t count = 0;
     KParams kp;
-    int rc = units_common(plan, u0, u1, grads_bucket, gdtype, begin, count, kp);
+    int rc = units_common(plan, u0, u1, grads_bucket, gdtype, true, count, kp);
     if (rc != ZERO_OK || count == 0) return rc;
     if ((rc = fill_state(plan, kp, master, m, v, pshard, full, pdtype, hp)) != ZERO_OK) return rc;
     return launch_pipe(MODE_FUSED, gdtype, count, kp, reinterpret_cast<cudaStream_t>(stream));
@@ -369,9 +391,9 @@ extern "C" int zero_step_units(const zero_plan *plan, int32_t u0, int32_t u1, co
 extern "C" int zero_clip_reduce_units(const zero_plan *plan, int32_t u0, int32_t u1, const void *const *grads_bucket,
                                       int32_t gdtype, float *const *gshard, zero_stream_t stream) {
     ZERO_NVTX_RANGE();
-    int64_t begin = 0, count = 0;
+    int64_t count = 0;
     KParams kp;
-    int rc = units_common(plan, u0, u1, grads_bucket, gdtype, begin, count, kp);
+    int rc = units_common(plan, u0, u1, grads_bucket, gdtype, false, count, kp);
     if (rc != ZERO_OK || count == 0) return rc;
     if ((rc = check_rank_ptrs(plan, reinterpret_cast<const void *const *>(gshard), true)) != ZERO_OK) return rc;
     kp.write_g = 1;
@@ -383,9 +405,9 @@ extern "C" int zero_clip_reduce_units(const zero_plan *plan, int32_t u0, int32_t
 extern "C" int zero_reduce_scatter_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit,
                                         int32_t gdtype, float *const *gshard, float coef, zero_stream_t stream) {
     ZERO_NVTX_RANGE();
-    int64_t begin = 0, count = 0;
+    int64_t count = 0;
     KParams kp;
-    int rc = unit_common(plan, unit, grads_unit, gdtype, begin, count, kp);
+    int rc = unit_common(plan, unit, grads_unit, gdtype, true, count, kp);
     if (rc != ZERO_OK || count == 0) return rc;
     if ((rc = check_rank_ptrs(plan, reinterpret_cast<const void *const *>(gshard), true)) != ZERO_OK) return rc;
     kp.coef = coef;
@@ -397,9 +419,9 @@ extern "C" int zero_reduce_scatter_unit(const zero_plan *plan, int32_t unit, con
 extern "C" int zero_clip_reduce_unit(const zero_plan *plan, int32_t unit, const void *const *grads_unit,
                                      int32_t gdtype, float *const *gshard, zero_stream_t stream) {
     ZERO_NVTX_RANGE();
-    int64_t begin = 0, count = 0;
+    int64_t count = 0;
     KParams kp;
-    int rc = unit_common(plan, unit, grads_unit, gdtype, begin, count, kp);
+    int rc = unit_common(plan, unit, grads_unit, gdtype, false, count, kp);
     if (rc != ZERO_OK || count == 0) return rc;
     if ((rc = check_rank_ptrs(plan, reinterpret_cast<const void *const *>(gshard), true)) != ZERO_OK) return rc;
     kp.write_g = 1;
@@ -432,6 +454,7 @@ extern "C" int zero_adamw_shard_step_clipped(const zero_plan *plan, const float 
     if ((rc = fill_state(plan, kp, master, m, v, pshard, full, pdtype, hp)) != ZERO_OK) return rc;
     for (int q = 0; q < plan->n_ranks; ++q) kp.gshard[q] = const_cast<float *>(gshard[q]);
     kp.seg_base = begin;
+    if (unit >= 0 && (rc = use_local_table(plan, unit, unit + 1, kp, count)) != ZERO_OK) return rc;
     kp.use_coef_dev = 1;  // the coefficient zero_clip_finalize left on the device (NaN: skip)
     kp.coef_dev = plan->d_coef;
     return launch_pipe(MODE_SHARD, ZERO_F32, count, kp, reinterpret_cast<cudaStream_t>(stream));

@@ -23,14 +23,23 @@ struct Seg {
 };
 static_assert(sizeof(Seg) == 32, "Seg must stay 32 bytes");
 
-// Longest segment: 8192 elements for up to 8 ranks, 32768 for more (measured:
+// Longest segment: 8192 elements for up to 8 ranks, 32256 for more (measured:
 // at N = 8 the shorter segments shorten the tail of every launch, which per-unit
-// and per-bucket launches pay each time; at N = 16 the pipeline's 1536-element
-// tile fits the longer segment better).  ZERO_SEG_MAX fixes one length for all
-// N (for measurements).  Segments after the first one of a slice start at a
+// and per-bucket launches pay each time; at N = 16 the longer segment fits the
+// pipeline better, and 32256 is 21 whole tiles of its 1536 elements, so a full
+// segment ends with no part-filled stage).  ZERO_SEG_MAX fixes one length for
+// all N (for measurements).  Segments after the first one of a slice start at a
 // shard position that is a multiple of 8, so 32-byte vector access needs no
 // peeling.
-constexpr int32_t kSegMaxSmallN = 8192, kSegMaxLargeN = 32768;
+constexpr int32_t kSegMaxSmallN = 8192, kSegMaxLargeN = 32256;
+
+// The unit-local launch table: the same slices cut so that each unit has about
+// kLocalSegsPerUnit segments (two per SM of a GB300) of at least kLocalSegMin
+// elements, at most the main table's length.  Launches over one unit or a run
+// of units without per-segment partial sums use it, so a small unit spreads
+// over every SM instead of one SM per slice; the element-wise results do not
+// depend on how the slices are cut.
+constexpr int64_t kLocalSegsPerUnit = 304, kLocalSegMin = 1024;
 inline int32_t seg_max_for(int32_t n_ranks) {
 #ifdef ZERO_SEG_MAX
     (void)n_ranks;
@@ -84,11 +93,14 @@ struct zero_plan {
     int64_t p_pad = 0, H = 0;
     std::vector<zero::Seg> segs;           // host copy of the launch table
     std::vector<int64_t> unit_seg_begin;   // [n_units + 1]: segments of unit u
+    std::vector<zero::Seg> segs_local;     // host copy of the unit-local launch table
+    std::vector<int64_t> unit_local_begin;  // [n_units + 1]: its segments of unit u
     std::vector<zero::UnitDesc> unit_table;  // host copy of the device unit table
     // device side, set by zero_plan_attach
     bool attached = false;
     int device = -1;
     zero::Seg *d_segs = nullptr;
+    zero::Seg *d_segs_local = nullptr;
     zero::SqPartial *d_partials = nullptr;  // kPartialSlots partial sums of squares per segment
     double *d_sqnorm = nullptr;     // S of the last clipped step
     float *d_coef = nullptr;        // clip coefficient of the last clipped step
@@ -106,7 +118,7 @@ constexpr int kFinBlocks = 128;
 
 // Workspace layout (byte offsets from the workspace base).
 struct WsLayout {
-    size_t segs, partials, scalars, units, fin, total;
+    size_t segs, partials, scalars, units, fin, segs_local, total;
 };
 WsLayout workspace_layout(const zero_plan *plan);
 int adam_consts(const zero_hparams *hp, AdamConsts *out);

@@ -23,7 +23,8 @@ WsLayout workspace_layout(const zero_plan *plan) {
     L.scalars = L.partials + round_up(nseg * zero::kPartialSlots * sizeof(zero::SqPartial), 256);
     L.units = L.scalars + 256;
     L.fin = L.units + round_up(plan->unit_table.size() * sizeof(UnitDesc), 256);
-    L.total = L.fin + round_up(zero::kFinBlocks * sizeof(double), 256);
+    L.segs_local = L.fin + round_up(zero::kFinBlocks * sizeof(double), 256);
+    L.total = L.segs_local + round_up(plan->segs_local.size() * sizeof(Seg), 256);
     return L;
 }
 
@@ -53,6 +54,44 @@ int adam_consts(const zero_hparams *hp, AdamConsts *out) {
     out->bc2 = bc2;
     out->eps = hp->eps;
     return ZERO_OK;
+}
+
+// Cuts unit u's N slices into segments of at most seg_len elements, appended to
+// table.  The first segment of a slice ends where the shard position reaches a
+// multiple of 8, so every later segment starts 32-byte aligned.
+static void cut_unit(const zero_plan *p, int32_t u, int64_t seg_len, std::vector<Seg> &table) {
+    const int64_t hu = p->h[u];
+    for (int32_t r = 0; r < p->n_ranks; ++r) {
+        int64_t j = 0;
+        while (j < hu) {
+            const int64_t s_off = p->Hoff[u] + j;
+            int64_t len = seg_len;
+            if (j == 0) len -= (s_off & 7);
+            if (len > hu - j) len = hu - j;
+            Seg sg;
+            sg.g_off = p->F[u] + static_cast<int64_t>(r) * hu + j;
+            sg.s_off = s_off;
+            sg.len = static_cast<int32_t>(len);
+            const int64_t unit_pos = static_cast<int64_t>(r) * hu + j;  // position inside the unit
+            int64_t valid = p->sizes[u] - unit_pos;
+            if (valid < 0) valid = 0;
+            if (valid > len) valid = len;
+            sg.valid = static_cast<int32_t>(valid);
+            sg.rank = r;
+            sg.unit = u;
+            table.push_back(sg);
+            j += len;
+        }
+    }
+}
+
+// Segment length of unit u in the unit-local table: about kLocalSegsPerUnit
+// segments, a multiple of 8, between kLocalSegMin and the main table's length.
+static int64_t local_seg_len(int64_t S, int64_t seg_max) {
+    int64_t len = (S + kLocalSegsPerUnit - 1) / kLocalSegsPerUnit;
+    len = (len + 7) / 8 * 8;
+    if (len < kLocalSegMin) len = kLocalSegMin;
+    return len < seg_max ? len : seg_max;
 }
 
 }  // namespace zero
@@ -108,37 +147,18 @@ extern "C" int zero_plan_create_aligned(const int64_t *unit_sizes, int32_t n_uni
         }
         p->p_pad = full;
         p->H = shard;
-        // Launch table: slices cut into segments of at most seg_max_for(N)
-        // elements; the first segment of a slice ends where the shard position
-        // reaches a multiple of 8, so every later segment starts 32-byte aligned.
+        // Launch tables: the main one, slices cut into segments of at most
+        // seg_max_for(N) elements, and the unit-local one.
         const int64_t seg_max = zero::seg_max_for(n_ranks);
+        p->unit_local_begin.resize(static_cast<size_t>(n_units) + 1);
         for (int32_t u = 0; u < n_units; ++u) {
             p->unit_seg_begin[u] = static_cast<int64_t>(p->segs.size());
-            const int64_t hu = p->h[u];
-            for (int32_t r = 0; r < n_ranks; ++r) {
-                int64_t j = 0;
-                while (j < hu) {
-                    const int64_t s_off = p->Hoff[u] + j;
-                    int64_t len = seg_max;
-                    if (j == 0) len -= (s_off & 7);
-                    if (len > hu - j) len = hu - j;
-                    Seg sg;
-                    sg.g_off = p->F[u] + static_cast<int64_t>(r) * hu + j;
-                    sg.s_off = s_off;
-                    sg.len = static_cast<int32_t>(len);
-                    const int64_t unit_pos = static_cast<int64_t>(r) * hu + j;  // position inside the unit
-                    int64_t valid = p->sizes[u] - unit_pos;
-                    if (valid < 0) valid = 0;
-                    if (valid > len) valid = len;
-                    sg.valid = static_cast<int32_t>(valid);
-                    sg.rank = r;
-                    sg.unit = u;
-                    p->segs.push_back(sg);
-                    j += len;
-                }
-            }
+            zero::cut_unit(p, u, seg_max, p->segs);
+            p->unit_local_begin[u] = static_cast<int64_t>(p->segs_local.size());
+            zero::cut_unit(p, u, zero::local_seg_len(p->S[u], seg_max), p->segs_local);
         }
         p->unit_seg_begin[n_units] = static_cast<int64_t>(p->segs.size());
+        p->unit_local_begin[n_units] = static_cast<int64_t>(p->segs_local.size());
         p->unit_table.resize(n_units);
         for (int32_t u = 0; u < n_units; ++u)
             p->unit_table[u] = zero::UnitDesc{p->F[u], p->S[u], p->h[u], p->Hoff[u], p->sizes[u], p->unit_seg_begin[u]};
@@ -183,6 +203,23 @@ extern "C" int zero_plan_segments(const zero_plan *plan, int64_t *out) {
     if (plan == nullptr || out == nullptr) return ZERO_EINVAL;
     for (size_t i = 0; i < plan->segs.size(); ++i) {
         const Seg &sg = plan->segs[i];
+        int64_t *o = out + 6 * i;
+        o[0] = sg.g_off;
+        o[1] = sg.s_off;
+        o[2] = sg.len;
+        o[3] = sg.valid;
+        o[4] = sg.rank;
+        o[5] = sg.unit;
+    }
+    return ZERO_OK;
+}
+
+extern "C" int zero_plan_local_segments(const zero_plan *plan, int64_t *n_segments, int64_t *out) {
+    if (plan == nullptr || n_segments == nullptr) return ZERO_EINVAL;
+    *n_segments = static_cast<int64_t>(plan->segs_local.size());
+    if (out == nullptr) return ZERO_OK;
+    for (size_t i = 0; i < plan->segs_local.size(); ++i) {
+        const Seg &sg = plan->segs_local[i];
         int64_t *o = out + 6 * i;
         o[0] = sg.g_off;
         o[1] = sg.s_off;

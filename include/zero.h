@@ -153,8 +153,19 @@ int zero_plan_counts(const zero_plan *plan, int32_t *n_units, int32_t *n_ranks, 
  * rank, unit}.  Segments are ordered by unit, then rank, then position. */
 int zero_plan_segments(const zero_plan *plan, int64_t *out);
 
-/* Bytes of device workspace the plan needs (work table, per-segment partial
- * sums, scalars). Host only. */
+/* The unit-local launch table, for inspection: the same slices cut so that each
+ * unit has about 304 segments (two per SM of a GB300) of at least 1024 elements
+ * and at most the main table's length.  Launches over one unit or a run of units
+ * that keep no per-segment partial sums use it (zero_step with unit >= 0,
+ * zero_step_unit, zero_step_units, zero_reduce_scatter_unit, the per-unit
+ * zero_adamw_shard_step_clipped and all-gathers), so a small unit spreads over
+ * every SM; results do not depend on the cut.  *n_segments (HOST) receives its
+ * length; out (HOST, 6 * that many int64, may be NULL) receives the segments in
+ * the layout of zero_plan_segments. */
+int zero_plan_local_segments(const zero_plan *plan, int64_t *n_segments, int64_t *out);
+
+/* Bytes of device workspace the plan needs (both work tables, per-segment
+ * partial sums, scalars). Host only. */
 int zero_plan_workspace_bytes(const zero_plan *plan, size_t *bytes);
 
 /* Binds the plan to the current device: copies its work table into the

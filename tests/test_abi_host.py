@@ -78,12 +78,22 @@ def test_aligned_plan_layout_matches_oracle(zlib, orc, sizes, N, align):
         assert (g - s) % align == 0 and (p.F[u] + r * p.h[u]) % align == 0
 
 
+@pytest.mark.parametrize("table", ["main", "local"])
 @pytest.mark.parametrize("align", [1, 8])
 @pytest.mark.parametrize("sizes,N", _units_cases()[:20])
-def test_launch_table_covers_every_slice_once(zlib, orc, sizes, N, align):
+def test_launch_table_covers_every_slice_once(zlib, orc, sizes, N, align, table):
+    """Both launch tables: the main one (whole-plan launches, norm passes) and the
+    unit-local one (one unit or a run of units, cut into about 304 segments each)."""
     p = Z.ZeroPlan(sizes, N, align=align)
-    segs = Z.zero_plan_segments(p.handle)
+    segs = Z.zero_plan_segments(p.handle) if table == "main" else Z.zero_plan_local_segments(p.handle)
     o = orc.Plan(sizes, N, align)
+    if table == "local":
+        seg_max = 8192 if N <= 8 else 32256
+        for u in range(len(sizes)):
+            n_u = sum(1 for sg in segs if sg[5] == u)
+            if o.S[u] >= 304 * 1024 and o.S[u] <= 304 * seg_max:
+                # about 304 per unit: each slice's first segment may be cut short by the alignment
+                assert 304 - N <= n_u <= 304 + 2 * N, (u, n_u)
     if o.P_pad == 0:
         assert segs == []
         return
@@ -91,7 +101,7 @@ def test_launch_table_covers_every_slice_once(zlib, orc, sizes, N, align):
     mp = o.shard_map()
     pad = o.pad_mask()
     for (g, s, ln, valid, r, u) in segs:
-        assert 1 <= ln <= 32768 and 0 <= valid <= ln
+        assert 1 <= ln <= 32256 and 0 <= valid <= ln
         covered[g:g + ln] += 1
         # the segment's full positions are exactly rank r's shard positions s..s+ln
         assert np.array_equal(mp[r, s:s + ln], np.arange(g, g + ln))
@@ -105,6 +115,26 @@ def test_launch_table_covers_every_slice_once(zlib, orc, sizes, N, align):
         g1, s1, l1, _, r1, u1 = segs[i]
         if (r0, u0) == (r1, u1):
             assert s1 == s0 + l0 and s1 % 8 == 0
+
+
+@pytest.mark.parametrize("N", [3, 8, 16])
+def test_local_table_spreads_small_units(zlib, N):
+    """The unit-local table cuts a unit of 2^20 elements into about 304 segments
+    (the main table: 128 at N = 8, 48 at N = 16), leaves large units as the main
+    table cuts them, and never goes below 1024 elements a segment except at the
+    end of a slice."""
+    sizes = [1000, 1 << 20, 64328960]
+    p = Z.ZeroPlan(sizes, N)
+    local, main = Z.zero_plan_local_segments(p.handle), Z.zero_plan_segments(p.handle)
+    per_unit = lambda segs, u: [sg for sg in segs if sg[5] == u]
+    assert 304 <= len(per_unit(local, 1)) <= 304 + 2 * N > len(per_unit(main, 1))
+    assert per_unit(local, 2) == per_unit(main, 2)
+    assert per_unit(local, 0) == per_unit(main, 0)  # a slice shorter than 1024 is one segment either way
+    h = p.h[1]
+    for (g, s, ln, valid, r, u) in per_unit(local, 1):
+        at_slice_end = g + ln == p.F[1] + (r + 1) * h
+        first = g == p.F[1] + r * h
+        assert ln >= 1024 - 7 or at_slice_end or first
 
 
 def test_named_workloads_layout(zlib, orc):
