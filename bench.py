@@ -421,8 +421,9 @@ def run_secondary(name, steps, warmup, dev):
 
 def per_unit_timing(plan, grads, master, m, v, full, steps, warmup, dev, stream, one_launch_ms):
     """The same unclipped step as one launch per unit instead of the one multi-unit launch:
-    launched from Python once, then captured in a CUDA graph and replayed (t fixed at
-    capture), each timed with CUDA events on the launching stream."""
+    launched from Python through zero_step, then through UnitSteps (arguments marshalled
+    once), then captured in a CUDA graph and replayed (t fixed at capture), each timed
+    with CUDA events on the launching stream."""
     import fsdp_sharded_optimizer_step_gb300 as Z
     from fsdp_sharded_optimizer_step_gb300 import workloads as W
 
@@ -444,6 +445,11 @@ def per_unit_timing(plan, grads, master, m, v, full, steps, warmup, dev, stream,
     unit_step(t)
     torch.cuda.synchronize(dev)
     python_ms = timed(lambda: unit_step(t), 1)
+    prepared = Z.UnitSteps(plan, grads, master, m, v, full=full)
+    hp_t = Z.AdamW(t=t, **W.HP)
+    prepared.step(hp_t)
+    torch.cuda.synchronize(dev)
+    prepared_ms = timed(lambda: prepared.step(hp_t), 1)
     graph = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream(dev)
     cap.wait_stream(stream)
@@ -456,6 +462,7 @@ def per_unit_timing(plan, grads, master, m, v, full, steps, warmup, dev, stream,
     graph_ms = timed(graph.replay, steps)
     del graph
     return {"launches_per_step": plan.n_units, "ms_launched_from_python": python_ms,
+            "ms_launched_from_python_marshalled_once": prepared_ms,
             "ms_replayed_from_cuda_graph": graph_ms, "one_launch_ms": one_launch_ms,
             "graph_vs_one_launch": graph_ms / one_launch_ms}
 

@@ -394,6 +394,37 @@ def zero_step(plan, grads, master, m, v, hp: AdamW, full=None, pshard=None, gsha
                            _stream(stream, plan.device)), "zero_step")
 
 
+class UnitSteps:
+    """The unclipped fused step as one zero_step launch per unit, with the tensors
+    checked and marshalled once: a per-unit loop from Python then costs one direct
+    C call per unit instead of a full binding call (rank-pointer arrays, dtype and
+    shape checks) each time.  The tensors must stay alive and in place while the
+    object is used."""
+
+    def __init__(self, plan, grads, master, m, v, full=None, pshard=None):
+        self.plan = plan
+        self._g, self._gd = _rows(plan, grads, plan.P_pad, "grads", _G)
+        self._w, _ = _rows(plan, master, plan.H, "master", _F)
+        self._m, _ = _rows(plan, m, plan.H, "m", _F)
+        self._v, _ = _rows(plan, v, plan.H, "v", _F)
+        self._fp, self._ps, self._pdt = _outputs(plan, full, pshard)
+        self._keep = (grads, master, m, v, full, pshard)
+        self._fn = lib().zero_step
+
+    def step(self, hp: AdamW, units=None, stream=None):
+        """Updates `units` (default: every unit, in order), one launch each."""
+        if hp.max_norm > 0:
+            raise ValueError("a clipped step needs every unit at once: use zero_step")
+        c = hp.c()
+        st = _stream(stream, self.plan.device)
+        h, fn = self.plan.handle, self._fn
+        for u in (range(self.plan.n_units) if units is None else units):
+            rc = fn(h, self._g, self._gd, self._w, self._m, self._v, self._fp, self._ps, self._pdt, None, C.byref(c),
+                    None, u, st)
+            if rc != ZERO_OK:
+                raise ZeroError(rc, "zero_step")
+
+
 def zero_grad_sqnorm_noalloc(grads, sqnorm_out, stream=None):
     """Sum of squares of the averaged gradient over flat rank buffers, with no
     device allocation (see include/zero.h); padding entries must hold 0."""

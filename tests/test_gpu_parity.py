@@ -240,6 +240,25 @@ def test_per_unit_launches_equal_one_multi_unit_launch():
     b.assert_pshard_equal()
 
 
+def test_unit_steps_marshalled_once_bit_exact():
+    """UnitSteps (arguments marshalled once, one direct zero_step call per unit, in any
+    order) against the oracle over three steps, with param shards and the full buffer;
+    a clipped step is refused."""
+    sizes = W.finewrap_units(n_units=40, lo_log2=0, hi_log2=16, seed=9) + [0, 70001]
+    c = SmallCase(sizes, 16, W.BF16, W.BF16, seed=41)
+    us = Z.UnitSteps(c.plan, c.grads, c.master, c.m, c.v, full=c.full, pshard=c.pshard)
+    order = list(range(len(sizes)))[::-1]
+    for t in (1, 2, 3):
+        hp, _ = hp_for(t)
+        us.step(hp, units=order if t == 2 else None)
+        assert c.oracle_step(t) == O.OK
+        c.assert_state_equal()
+        c.assert_full_equal()
+        c.assert_pshard_equal()
+    with pytest.raises(ValueError):
+        us.step(hp_for(4, 1.0)[0])
+
+
 def test_per_unit_steps_replay_from_a_cuda_graph():
     """The per-unit launches of one step captured in a CUDA graph (the library
     makes no synchronising or allocating call on that path) and replayed: the
