@@ -204,6 +204,17 @@ class SmallCase:
         assert bad.size == 0, f"pshard: {bad.shape[0]} differ, first at {bad[0]}"
 
 
+def segment_edges(plan) -> np.ndarray:
+    """The first and last full position of every segment of the library's two launch
+    tables (where a CTA's work, a head, a tail or a tile begins or ends)."""
+    out = []
+    for segs in (Z.zero_plan_segments(plan.handle), Z.zero_plan_local_segments(plan.handle)):
+        if segs:
+            a = np.array(segs, dtype=np.int64)
+            out += [a[:, 0], a[:, 0] + a[:, 2] - 1]
+    return np.unique(np.concatenate(out)) if out else np.zeros(0, np.int64)
+
+
 def sample_positions(plan_o: "O.Plan", n_random, seed, extra_units=(), extra_pos=()):
     """Seeded random full positions plus every unit's first/last element, every
     slice boundary and ragged tail, the given extra positions, and all positions
@@ -218,7 +229,7 @@ def sample_positions(plan_o: "O.Plan", n_random, seed, extra_units=(), extra_pos
             continue
         b = [F, F + S - 1, F + int(plan_o.sizes[u]) - 1 if plan_o.sizes[u] > 0 else F]
         for r in range(N):
-            b += [F + r * h, F + r * h + h - 1, min(F + r * h + 7, F + S - 1), min(F + r * h + 32768, F + S - 1)]
+            b += [F + r * h, F + r * h + h - 1, min(F + r * h + 7, F + S - 1)]
         pos.append(np.array(b, np.int64))
     pos = np.unique(np.concatenate(pos))
     pos = pos[(pos >= 0) & (pos < P)]
@@ -259,6 +270,7 @@ class SampledCase:
         self.gshard = Z.rank_buffers(N, H, torch.float32, self.device) if self.clip else None
         self.sq = torch.zeros(1, dtype=torch.float64, device=self.device)
         # the sample
+        extra_pos = np.concatenate([np.asarray(extra_pos, np.int64), segment_edges(self.plan)])
         self.pos = sample_positions(self.o, n_random, seed, extra_units, extra_pos)
         self.rank, self.spos, self.padflag = self.o.locate(self.pos)
         pos_t = torch.from_numpy(self.pos).to(self.device)
