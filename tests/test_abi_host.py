@@ -261,6 +261,19 @@ def test_binding_refuses_wrong_tensors_on_the_host(zlib):
                               torch.zeros(2, p.H, dtype=torch.float32))
 
 
+def test_unit_steps_checks_its_tensors_once_on_the_host(zlib):
+    """UnitSteps validates and marshals its tensors at construction (a wrong shape,
+    dtype or device raises there, before any launch)."""
+    import torch
+    p = Z.ZeroPlan([10, 3], 2)  # host-only plan: no device, so CPU tensors are refused too
+    g = torch.zeros(2, p.P_pad, dtype=torch.bfloat16)
+    st = [torch.zeros(2, p.H) for _ in range(3)]
+    with pytest.raises(ValueError):
+        Z.UnitSteps(p, g, *st)
+    with pytest.raises(ValueError):
+        Z.UnitSteps(p, g[:, :-1], *st)
+
+
 def test_rank_pointers_of_a_2d_tensor_match_its_rows():
     """The binding takes the N rank pointers of a [N, L] tensor from its row stride;
     they must be the pointers of its rows (padded rows, views, empty buffers)."""
